@@ -1,0 +1,473 @@
+"""Benchmark of the paged KV-cache attention hot path on one GB300 per rank.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl pkv|reference]
+
+A step is one pass of the hot path over one batch: kv_store of the step's new
+tokens, then attention over the paged cache.  The headline step is the decode
+batch (64 sequences, contexts U[128, 2048], 16 q / 8 kv heads, D=128, a
+1024-block pool): value = algorithmic HBM bytes (valid-context K/V + q + out +
+the store's rows) / step time.  The same line carries the prefill (varlen
+causal, TFLOP/s), long skewed decode and prefix-cached prefill workloads, the
+decode kernel's roofline, an end-to-end number through host buffers, clocks,
+and the CPU oracle's speed on this host.
+
+Caches rotate over several copies so that consecutive steps never find their
+working set in L2 (each copy is larger than the 129 MB L2 or the rotation
+spans well over it).
+
+--impl reference times the fp64 CPU oracle (the only other implementation of
+the path) on this host on a bounded sample of the same workload.
+"""
+import os
+
+# The CPU oracle is timed single-threaded: pin BLAS/OpenMP before numpy loads.
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse
+import json
+import math
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "paged decode-attn HBM GB/s (% of peak); prefill attn TFLOP/s (% of peak)"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in PEAKS_FALLBACK}, "measured"
+    except Exception:
+        return dict(PEAKS_FALLBACK), "fallback"
+
+
+# ------------------------------------------------------------ work counting
+
+def decode_bytes(b):
+    """Algorithmic bytes of decode attention: valid-context K and V, q, out."""
+    kv = int(np.sum(b.context_lens.astype(np.int64))) * b.num_kv_heads * b.head_dim * 2 * 2
+    qo = 2 * b.num_seqs * b.num_q_heads * b.head_dim * 2
+    return kv + qo
+
+
+def store_bytes(b):
+    """kv_store moves each new K and V row in and out once."""
+    return int(b.k.shape[0]) * b.num_kv_heads * b.head_dim * 2 * 2 * 2
+
+
+def prefill_flops(b):
+    """4*D*Hq per unmasked (query, key) pair."""
+    c = b.cached_lens.astype(np.int64)
+    n = b.new_lens.astype(np.int64)
+    pairs = int(np.sum(n * c + n * (n + 1) // 2))
+    return 4 * b.head_dim * b.num_q_heads * pairs
+
+
+def prefill_bytes(b):
+    """q + out + each sequence's K/V read once."""
+    kv = int(np.sum(b.context_lens.astype(np.int64))) * b.num_kv_heads * b.head_dim * 2 * 2
+    return kv + 2 * int(b.q.shape[0]) * b.num_q_heads * b.head_dim * 2
+
+
+# ------------------------------------------------------------ clock sampling
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_id), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ GPU arm
+
+def device_batch(b, dev, fill_cache_on_device, seed):
+    """Upload a batch; when the cache was not materialised on the host, fill
+    the used blocks on the device with seeded N(0,1) bf16 (same distribution)."""
+    import torch
+
+    t = {}
+
+    def bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    def i32(a):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+
+    t["q"] = bf16(b.q)
+    t["k"] = bf16(b.k)
+    t["v"] = bf16(b.v)
+    t["slot_mapping"] = i32(b.slot_mapping)
+    t["block_tables"] = i32(b.block_tables)
+    t["context_lens"] = i32(b.context_lens)
+    t["cu_q"] = i32(b.cu_seqlens_q)
+    t["cu_k"] = i32(b.cu_seqlens_k)
+    shape = (b.num_blocks, b.block_size, b.num_kv_heads, b.head_dim)
+    if b.k_cache is not None:
+        t["k_cache"] = bf16(b.k_cache)
+        t["v_cache"] = bf16(b.v_cache)
+    else:
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed)
+        t["k_cache"] = torch.randn(shape, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+        t["v_cache"] = torch.randn(shape, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    return t
+
+
+def clone_batch(t):
+    return {k: v.clone() for k, v in t.items()}
+
+
+class Arm:
+    """Runs one workload's step on the GPU with rotation over cache copies."""
+
+    def __init__(self, pkv, b, dev, copies):
+        import torch
+
+        self.pkv, self.b, self.dev = pkv, b, dev
+        base = device_batch(b, dev, b.k_cache is None, b.seed)
+        self.copies = [base] + [clone_batch(base) for _ in range(copies - 1)]
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.mtb = b.total_blocks_used
+        if b.kind == "decode":
+            self.ws = [pkv.decode_workspace(b.num_seqs, b.num_q_heads, b.num_kv_heads, b.head_dim,
+                                            self.mtb, dev) for _ in range(copies)]
+            self.out = [torch.empty((b.num_seqs, b.num_q_heads, b.head_dim), dtype=torch.bfloat16,
+                                    device=dev) for _ in range(copies)]
+        else:
+            self.out = [torch.empty((b.q.shape[0], b.num_q_heads, b.head_dim),
+                                    dtype=torch.bfloat16, device=dev) for _ in range(copies)]
+        self.max_q = int(b.new_lens.max())
+        torch.cuda.synchronize()
+
+    def store(self, i):
+        t = self.copies[i % len(self.copies)]
+        self.pkv.kv_store(t["k"], t["v"], t["k_cache"], t["v_cache"], t["slot_mapping"],
+                          self.status)
+
+    def attend(self, i):
+        r = i % len(self.copies)
+        t = self.copies[r]
+        b = self.b
+        if b.kind == "decode":
+            self.pkv.paged_decode_attn(self.out[r], t["q"], t["k_cache"], t["v_cache"],
+                                       t["block_tables"], t["context_lens"], b.scale, self.ws[r],
+                                       self.mtb, self.status)
+        else:
+            self.pkv.paged_prefill_attn(self.out[r], t["q"], t["k_cache"], t["v_cache"],
+                                        t["block_tables"], t["cu_q"], t["cu_k"], self.max_q,
+                                        b.scale, self.status)
+
+    def run(self, steps, warmup):
+        """Time `steps` steps; returns (total ms, mean attention-kernel ms, mean store ms)."""
+        import torch
+
+        stream = torch.cuda.current_stream()
+        for i in range(warmup):
+            self.store(i)
+            self.attend(i)
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+               torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(steps):
+            e0, e1, e2 = ev[i]
+            e0.record(stream)
+            self.store(i)
+            e1.record(stream)
+            self.attend(i)
+            e2.record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        total = t0.elapsed_time(t1)
+        store_ms = sum(e0.elapsed_time(e1) for e0, e1, _ in ev) / steps
+        attn_ms = sum(e1.elapsed_time(e2) for _, e1, e2 in ev) / steps
+        if int(self.status.item()) != 0:
+            raise RuntimeError(f"device status {int(self.status.item()):#x} on {self.b.name}")
+        return total, attn_ms, store_ms
+
+
+def e2e_decode(pkv, b, dev, steps, warmup):
+    """Decode step through host buffers: per step copy the step's inputs from
+    pinned host memory, store + attend, copy the output back."""
+    import torch
+
+    t = device_batch(b, dev, b.k_cache is None, b.seed)
+    host = {k: t[k].cpu().pin_memory() for k in ("q", "k", "v", "slot_mapping", "block_tables",
+                                                   "context_lens")}
+    out_host = torch.empty((b.num_seqs, b.num_q_heads, b.head_dim), dtype=torch.bfloat16).pin_memory()
+    out = torch.empty((b.num_seqs, b.num_q_heads, b.head_dim), dtype=torch.bfloat16, device=dev)
+    mtb = b.total_blocks_used
+    ws = pkv.decode_workspace(b.num_seqs, b.num_q_heads, b.num_kv_heads, b.head_dim, mtb, dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def step():
+        for k, v in host.items():
+            t[k].copy_(v, non_blocking=True)
+        pkv.kv_store(t["k"], t["v"], t["k_cache"], t["v_cache"], t["slot_mapping"], status)
+        pkv.paged_decode_attn(out, t["q"], t["k_cache"], t["v_cache"], t["block_tables"],
+                              t["context_lens"], b.scale, ws, mtb, status)
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        step()
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / steps
+    return ms, h2d, d2h
+
+
+# ------------------------------------------------------------ oracle timing
+
+def oracle_decode_timing(b, budget_s=8.0):
+    """Time the fp64 CPU oracle on whole decode steps of batch b (single thread)."""
+    import oracle
+
+    kc, vc = b.k_cache, b.v_cache
+    passes = 0
+    t0 = time.perf_counter()
+    while True:
+        kc2, vc2 = oracle.kv_store(kc, vc, b.k, b.v, b.slot_mapping)
+        oracle.paged_decode_attn(b.q, kc2, vc2, b.block_tables, b.context_lens, b.scale)
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or passes >= 50:
+            break
+    return el / passes, passes
+
+
+def oracle_sample_batch():
+    """Bounded sample of the decode workload for the CPU oracle: the first 16
+    of its 64 sequences (cache materialised on the host)."""
+    full = wl.decode(fill_cache=False)
+    n = 16
+    return wl.build_batch("decode-sample", "decode", 2, full.cached_lens[:n], full.new_lens[:n],
+                          full.num_q_heads, full.num_kv_heads, full.head_dim,
+                          num_blocks=sum(wl.blocks_for(L) for L in full.context_lens[:n]))
+
+
+# ------------------------------------------------------------ main
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+
+    b = oracle_sample_batch()
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        kc, vc = oracle.kv_store(b.k_cache, b.v_cache, b.k, b.v, b.slot_mapping)
+        oracle.paged_decode_attn(b.q, kc, vc, b.block_tables, b.context_lens, b.scale)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    per = sum(times) / len(times)
+    gbs = (decode_bytes(b) + store_bytes(b)) / per / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "decode: 16 of the 64 sequences of the decode batch "
+                               "(contexts U[128,2048], 16 q / 8 kv heads, D=128, block 256)",
+                   "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": "16 of 64 decode sequences per step"},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only-main", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+
+    import paged_kv_cache_241_gb300 as pkv
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as tdist
+
+        tdist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pkv.load()
+    peaks, peak_src = load_peaks()
+    props = torch.cuda.get_device_properties(dev)
+    gpu_index = getattr(props, "uuid", None)
+    sampler = ClockSampler(f"GPU-{gpu_index}" if gpu_index else local)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+
+    # ---- headline: decode batch (4 rotating copies of the 1 GiB pool) ----
+    b = wl.decode(fill_cache=False)
+    arm = Arm(pkv, b, dev, copies=4)
+    sampler.start()
+    barrier()
+    total_ms, attn_ms, store_ms = arm.run(args.steps, args.warmup)
+    barrier()
+    total_ms = max_over_ranks(total_ms)
+    ms_step = total_ms / args.steps
+    step_bytes = decode_bytes(b) + store_bytes(b)
+    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+    achieved = decode_bytes(b) / (attn_ms * 1e-3) / 1e9
+    extra = {}
+    if not args.only_main:
+        # ---- other workloads of the path ----
+        for name, make, copies, steps in (("longdecode", wl.longdecode, 3, 200),
+                                          ("prefill", wl.prefill, 4, 100),
+                                          ("prefix", wl.prefix, 8, 300)):
+            bb = make(fill_cache=False)
+            a2 = Arm(pkv, bb, dev, copies=copies)
+            tot, am, sm_ = a2.run(steps, args.warmup)
+            rec = {"ms_per_step": tot / steps, "attn_kernel_ms": am, "kv_store_ms": sm_}
+            if bb.kind == "decode":
+                ach = decode_bytes(bb) / (am * 1e-3) / 1e9
+                rec["roofline"] = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"],
+                                   "unit": "GB/s", "frac": ach / peaks["hbm_gbs"]}
+            else:
+                tf = prefill_flops(bb) / (am * 1e-3) / 1e12
+                rec["tflops"] = tf
+                rec["roofline"] = {"bound": "tensor", "achieved": tf,
+                                   "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                                   "frac": tf / peaks["bf16_tflops"]}
+                kvb = store_bytes(bb) / (sm_ * 1e-3) / 1e9
+                rec["kv_store"] = {"GB/s": kvb, "frac": kvb / peaks["hbm_gbs"],
+                                   "bytes": store_bytes(bb)}
+            extra[name] = rec
+            del a2
+            torch.cuda.empty_cache()
+    clocks = sampler.stop()
+    del arm
+    torch.cuda.empty_cache()
+
+    # ---- end to end through host buffers ----
+    e2e_ms, h2d, d2h = e2e_decode(pkv, b, dev, max(50, args.steps // 10), args.warmup)
+    e2e_val = world * step_bytes / (e2e_ms * 1e-3) / 1e9
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "decode: 64 seqs, contexts U[128,2048], 16 q / 8 kv heads, D=128, "
+                               "block 256, 1024-block permuted pool; kv_store of 64 tokens + "
+                               "paged decode attention per step",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "4 rotating cache copies (4.3 GB) between consecutive steps",
+                   "step_bytes": step_bytes},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "kernel": "paged_decode_kernel<128,2>", "peak_source": peak_src,
+                     "attn_kernel_ms": attn_ms, "kv_store_ms": store_ms},
+        "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+    }
+    line.update(extra)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sb = oracle_sample_batch()
+        per, passes = oracle_decode_timing(sb)
+        line["cpu_baseline"] = {"value": (decode_bytes(sb) + store_bytes(sb)) / per / 1e9,
+                                "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                "sample": f"16 of the 64 decode sequences, {passes} passes, "
+                                          f"{per:.2f} s per pass"}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,168 @@
+/*
+ * pkv.h -- C ABI of the paged KV-cache attention library (GB300, sm_103a).
+ *
+ * The operations are those of a nano-vllm style engine's attention layer:
+ *   - the KV-cache store through a slot mapping, which nano-vllm performs with
+ *     a Triton kernel (nano-vllm hub page, pomoai.com, "core tech 2:
+ *     Attention + Triton kernel");
+ *   - attention over the paged cache, with fixed 256-token blocks managed by a
+ *     block manager (same page, "core tech 4: KV Cache block manager") and a
+ *     per-sequence block table mapping logical to physical blocks (CSDN essay
+ *     "from nanoVLLM to vLLM", Mountain 1: KV cache);
+ *   - separate kernels for the compute-dense prefill phase and the
+ *     memory-bound decode phase (same essay, Mountain 3 and the study route's
+ *     attention/ module notes).
+ * The result of both attention calls is that of standard attention,
+ * softmax(q K^T * scale) V: FlashAttention-style tiling only reorders the
+ * computation (same essay, Mountain 3).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - bf16 tensors are passed as pointers to their 16-bit patterns.
+ *  - Every pointer argument except `dev_status` and `stream` is a DEVICE
+ *    pointer owned by the caller; the library allocates no memory, keeps no
+ *    reference after the call returns, and only caches small per-device
+ *    tables (the SM count).
+ *  - Layouts (all row-major, contiguous):
+ *      q             [T_q, Hq, D]
+ *      k, v          [T_new, Hkv, D]   (token stride configurable in kv_store)
+ *      k_cache       [num_blocks, block_size, Hkv, D]; one slot = Hkv*D values
+ *      v_cache       same as k_cache
+ *      out           [T_q, Hq, D]
+ *      block_tables  int32 [num_seqs, max_blocks_per_seq], unused entries -1
+ *      slot_mapping  int32 [T_new]; slot = block * block_size + offset; -1 = skip
+ *      context_lens  int32 [num_seqs]; keys visible, INCLUDING the tokens just
+ *                    stored
+ *      cu_seqlens_q  int32 [num_seqs+1], prefix sums of new-token counts
+ *      cu_seqlens_k  int32 [num_seqs+1], prefix sums of (cached + new) counts
+ *  - GQA: query head h reads kv head h / (Hq / Hkv).
+ *  - Pointers to bf16 data must be 16-byte aligned.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
+ *    legacy default stream).  Host-side argument checks run before any
+ *    launch: a failed check returns a status and launches nothing.
+ *  - Data-dependent faults (a slot or block id out of range, an empty or
+ *    oversize context) are caught by bounds checks on the device: the kernel
+ *    skips the access, ORs a PKV_DEV_* bit into *dev_status (when dev_status is
+ *    not NULL; it is a device int32) and finishes.  Nothing traps or spins
+ *    without a limit; a wait that exceeds its limit sets PKV_DEV_TIMEOUT.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pkv_status {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer */
+  PKV_ERR_UNSUPPORTED = 2, /* head_dim, group size or block_size not built */
+  PKV_ERR_WORKSPACE = 3,   /* workspace missing or too small */
+  PKV_ERR_CUDA = 4         /* a CUDA runtime/driver call or launch failed */
+} pkv_status;
+
+/* Bits OR-ed into *dev_status by the kernels. */
+#define PKV_DEV_BAD_SLOT 0x1    /* slot_mapping entry outside [-1, NB*BS) */
+#define PKV_DEV_BAD_BLOCK 0x2   /* block_tables entry outside [0, NB) */
+#define PKV_DEV_BAD_CONTEXT 0x4 /* context length <= 0 or > max_blocks*BS */
+#define PKV_DEV_TIMEOUT 0x8     /* a bounded wait ran out */
+#define PKV_DEV_WORKSPACE 0x10  /* decode: more blocks than max_total_blocks */
+#define PKV_DEV_BAD_SEQLEN 0x20 /* prefill: bad cu_seqlens (n > len_k, n > max_seqlen_q) */
+
+/* Human-readable name of a pkv_status value (static string). */
+const char *pkv_status_string(int status);
+
+/* ABI revision of this header; bumped on any signature change. */
+int pkv_abi_version(void);
+
+/*
+ * kv_store -- write this step's new K and V rows into the paged cache.
+ *
+ * For every token t in [0, num_tokens) with s = slot_mapping[t] >= 0:
+ *   k_cache slot s (Hkv*D values) <- k row t,  v_cache slot s <- v row t.
+ * A bit copy: no arithmetic touches the values.  Slots equal to -1 are
+ * skipped (padding); any other slot outside [0, num_blocks*block_size) sets
+ * PKV_DEV_BAD_SLOT and is skipped.  Slots >= 0 must be unique.
+ *
+ * k_token_stride / v_token_stride: elements between consecutive tokens of k
+ * and v (0 = Hkv*D, i.e. contiguous); must keep rows 16-byte aligned.
+ * Requires (Hkv*D) % 8 == 0.
+ */
+pkv_status pkv_kv_store(const uint16_t *k, const uint16_t *v, uint16_t *k_cache,
+                        uint16_t *v_cache, const int32_t *slot_mapping, int64_t num_tokens,
+                        int num_kv_heads, int head_dim, int64_t k_token_stride,
+                        int64_t v_token_stride, int64_t num_blocks, int block_size,
+                        int32_t *dev_status, void *stream);
+
+/*
+ * Bytes of device workspace paged_decode_attn needs.  max_total_blocks is an
+ * upper bound the caller guarantees on sum_s ceil(context_lens[s]/block_size)
+ * (num_seqs * max_blocks_per_seq always works).
+ */
+size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                 int64_t max_total_blocks);
+
+/*
+ * paged_decode_attn -- one query token per sequence against its paged K/V.
+ *
+ * out[s, h, :] = softmax_p(scale * <q[s,h,:], K_s[p, h/g, :]>) V_s[p, h/g, :]
+ * over p in [0, context_lens[s]), where K_s[p] is the cache slot
+ * block_tables[s][p / block_size] * block_size + p % block_size and
+ * g = Hq / Hkv.  bf16 in, fp32 accumulation, bf16 out (round to nearest even).
+ *
+ * Split-K flash-decoding: each (sequence, kv head, block) is one work item
+ * whose partial (max, sum, unnormalised output) goes to the workspace; the
+ * last item of a (sequence, kv head) to finish merges them.
+ *
+ * workspace: device buffer of at least pkv_decode_workspace_size(...) bytes,
+ * 256-byte aligned, ZERO-FILLED before its first use.  Every call leaves its
+ * counters at zero again, so it can be reused without clearing; after a call
+ * that reported PKV_DEV_TIMEOUT, zero it again.  Calls that overlap on the
+ * device must not share a workspace.
+ *
+ * Supported: head_dim in {64, 128}; Hq/Hkv in {1, 2, 4, 8}; block_size in
+ * {64, 128, 256, 512}; num_seqs <= 16384.
+ */
+pkv_status pkv_paged_decode_attn(uint16_t *out, const uint16_t *q, const uint16_t *k_cache,
+                                 const uint16_t *v_cache, const int32_t *block_tables,
+                                 const int32_t *context_lens, int num_seqs, int num_q_heads,
+                                 int num_kv_heads, int head_dim, int block_size,
+                                 int max_blocks_per_seq, int64_t num_blocks,
+                                 int64_t max_total_blocks, float scale, void *workspace,
+                                 size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/*
+ * paged_prefill_attn -- causal attention of packed variable-length prompts
+ * over the paged cache, including an already-cached prefix.
+ *
+ * For sequence s: n = cu_seqlens_q[s+1] - cu_seqlens_q[s] new queries and
+ * len_k = cu_seqlens_k[s+1] - cu_seqlens_k[s] keys, of which c = len_k - n
+ * were cached before this step (their K/V, and the new tokens' K/V, must
+ * already be in the cache: call kv_store first).  Query i sits at absolute
+ * position c + i and attends to keys 0 .. c + i:
+ *   out[cu_q[s]+i, h, :] = softmax_{p <= c+i}(scale * <q, K_s[p, h/g]>) V_s[p, h/g]
+ * bf16 operands on the tcgen05 tensor cores, fp32 accumulation in tensor
+ * memory, bf16 out.
+ *
+ * total_q = cu_seqlens_q[num_seqs]; max_seqlen_q bounds every n (a larger n
+ * sets PKV_DEV_BAD_SEQLEN and its excess rows are not written).
+ *
+ * Supported: head_dim in {64, 128}; Hq/Hkv in {1, 2, 4, 8};
+ * block_size in {64, 128, 256, 512}.
+ */
+pkv_status pkv_paged_prefill_attn(uint16_t *out, const uint16_t *q, const uint16_t *k_cache,
+                                  const uint16_t *v_cache, const int32_t *block_tables,
+                                  const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                                  int num_seqs, int64_t total_q, int max_seqlen_q,
+                                  int num_q_heads, int num_kv_heads, int head_dim,
+                                  int block_size, int max_blocks_per_seq, int64_t num_blocks,
+                                  float scale, int32_t *dev_status, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

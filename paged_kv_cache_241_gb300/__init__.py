@@ -1,0 +1,191 @@
+"""Paged KV-cache attention for GB300 (sm_103a): Python binding of libpkv.
+
+A thin ctypes layer over the C ABI declared in include/pkv.h.  It only
+marshals arguments (torch tensors -> device pointers and sizes, the current
+CUDA stream) and raises on a non-OK status; every step of the computation runs
+in the library's CUDA kernels.  There is no CPU fallback: if the shared library
+has not been built, `load()` raises.
+
+    import paged_kv_cache_241_gb300 as pkv
+    pkv.kv_store(k, v, k_cache, v_cache, slot_mapping)
+    pkv.paged_decode_attn(out, q, k_cache, v_cache, block_tables, context_lens,
+                          scale, workspace, max_total_blocks)
+    pkv.paged_prefill_attn(out, q, k_cache, v_cache, block_tables, cu_q, cu_k,
+                           max_seqlen_q, scale)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpkv.so")
+
+PKV_OK = 0
+STATUS_NAMES = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED",
+                3: "PKV_ERR_WORKSPACE", 4: "PKV_ERR_CUDA"}
+DEV_BAD_SLOT = 0x1
+DEV_BAD_BLOCK = 0x2
+DEV_BAD_CONTEXT = 0x4
+DEV_TIMEOUT = 0x8
+DEV_WORKSPACE = 0x10
+DEV_BAD_SEQLEN = 0x20
+
+# Exported symbols and their ctypes signatures (must match include/pkv.h).
+_c_int, _c_i64, _c_sz, _c_f, _p = (ctypes.c_int, ctypes.c_int64, ctypes.c_size_t,
+                                   ctypes.c_float, ctypes.c_void_p)
+SIGNATURES = {
+    "pkv_status_string": (ctypes.c_char_p, [_c_int]),
+    "pkv_abi_version": (_c_int, []),
+    "pkv_kv_store": (_c_int, [_p, _p, _p, _p, _p, _c_i64, _c_int, _c_int, _c_i64, _c_i64, _c_i64,
+                              _c_int, _p, _p]),
+    "pkv_decode_workspace_size": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_i64]),
+    "pkv_paged_decode_attn": (_c_int, [_p, _p, _p, _p, _p, _p, _c_int, _c_int, _c_int, _c_int,
+                                       _c_int, _c_int, _c_i64, _c_i64, _c_f, _p, _c_sz, _p, _p]),
+    "pkv_paged_prefill_attn": (_c_int, [_p, _p, _p, _p, _p, _p, _p, _c_int, _c_i64, _c_int,
+                                        _c_int, _c_int, _c_int, _c_int, _c_int, _c_i64, _c_f, _p,
+                                        _p]),
+}
+
+_lib = None
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what} failed: {STATUS_NAMES.get(status, status)}")
+        self.status = status
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libpkv.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build it with `python -m paged_kv_cache_241_gb300.build` "
+            "(the CUDA library is required; there is no fallback)")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(status: int, what: str) -> None:
+    if status != PKV_OK:
+        raise PkvError(status, what)
+
+
+def _stream(stream) -> int:
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(getattr(stream, "cuda_stream", stream))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t, dtype, name, ndim=None):
+    import torch
+
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name}: expected {ndim} dims, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    return t
+
+
+def kv_store(k, v, k_cache, v_cache, slot_mapping, dev_status=None, stream=None) -> None:
+    """Write new K/V rows k/v [T, Hkv, D] (bf16; rows may be strided by a
+    token stride) into k_cache/v_cache [NB, BS, Hkv, D] at slot_mapping [T]."""
+    import torch
+
+    lib = load()
+    _need(k_cache, torch.bfloat16, "k_cache", 4)
+    _need(v_cache, torch.bfloat16, "v_cache", 4)
+    _need(slot_mapping, torch.int32, "slot_mapping", 1)
+    NB, BS, Hkv, D = k_cache.shape
+    for name, t in (("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 3:
+            raise ValueError(f"{name}: expected a CUDA bf16 [T, Hkv, D] tensor")
+        if t.stride(2) != 1 or t.stride(1) != D or tuple(t.shape[1:]) != (Hkv, D):
+            raise ValueError(f"{name}: rows must be contiguous [Hkv, D] = {(Hkv, D)}")
+    st = lib.pkv_kv_store(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping),
+                          k.shape[0], Hkv, D, k.stride(0), v.stride(0), NB, BS,
+                          _ptr(dev_status), _stream(stream))
+    _check(st, "pkv_kv_store")
+
+
+def decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_total_blocks) -> int:
+    return int(load().pkv_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                max_total_blocks))
+
+
+def decode_workspace(num_seqs, num_q_heads, num_kv_heads, head_dim, max_total_blocks,
+                     device="cuda"):
+    """Allocate a zero-filled decode workspace (uint8, 256-byte aligned by torch)."""
+    import torch
+
+    n = decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_total_blocks)
+    return torch.zeros(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def paged_decode_attn(out, q, k_cache, v_cache, block_tables, context_lens, scale, workspace,
+                      max_total_blocks, dev_status=None, stream=None) -> None:
+    """out/q [S, Hq, D] bf16; block_tables [S, max_blocks] int32; context_lens [S] int32."""
+    import torch
+
+    lib = load()
+    _need(out, torch.bfloat16, "out", 3)
+    _need(q, torch.bfloat16, "q", 3)
+    _need(k_cache, torch.bfloat16, "k_cache", 4)
+    _need(v_cache, torch.bfloat16, "v_cache", 4)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(context_lens, torch.int32, "context_lens", 1)
+    S, Hq, D = q.shape
+    NB, BS, Hkv, Dc = k_cache.shape
+    if Dc != D or tuple(out.shape) != (S, Hq, D) or block_tables.shape[0] != S or \
+            context_lens.shape[0] != S or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("paged_decode_attn: inconsistent shapes")
+    st = lib.pkv_paged_decode_attn(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+        _ptr(context_lens), S, Hq, Hkv, D, BS, block_tables.shape[1], NB, int(max_total_blocks),
+        float(scale), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(dev_status), _stream(stream))
+    _check(st, "pkv_paged_decode_attn")
+
+
+def paged_prefill_attn(out, q, k_cache, v_cache, block_tables, cu_seqlens_q, cu_seqlens_k,
+                       max_seqlen_q, scale, dev_status=None, stream=None) -> None:
+    """out/q [T, Hq, D] bf16 packed by cu_seqlens_q; keys from the paged cache."""
+    import torch
+
+    lib = load()
+    _need(out, torch.bfloat16, "out", 3)
+    _need(q, torch.bfloat16, "q", 3)
+    _need(k_cache, torch.bfloat16, "k_cache", 4)
+    _need(v_cache, torch.bfloat16, "v_cache", 4)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(cu_seqlens_q, torch.int32, "cu_seqlens_q", 1)
+    _need(cu_seqlens_k, torch.int32, "cu_seqlens_k", 1)
+    T, Hq, D = q.shape
+    NB, BS, Hkv, Dc = k_cache.shape
+    S = cu_seqlens_q.shape[0] - 1
+    if Dc != D or tuple(out.shape) != (T, Hq, D) or block_tables.shape[0] != S or \
+            cu_seqlens_k.shape[0] != S + 1 or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("paged_prefill_attn: inconsistent shapes")
+    st = lib.pkv_paged_prefill_attn(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(cu_seqlens_q),
+        _ptr(cu_seqlens_k), S, T, int(max_seqlen_q), Hq, Hkv, D, BS, block_tables.shape[1], NB,
+        float(scale), _ptr(dev_status), _stream(stream))
+    _check(st, "pkv_paged_prefill_attn")

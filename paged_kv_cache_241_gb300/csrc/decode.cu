@@ -1,0 +1,696 @@
+// decode.cu -- paged decode attention: split-K flash-decoding over a block table.
+//
+// Decode attends one new query token per sequence to the whole paged context;
+// each step re-reads the sequence's cached keys and values, so it is bound by
+// memory bandwidth (CSDN essay "from nanoVLLM to vLLM", Mountain 3 and the
+// study route's note on the attention/ module).  The context lives in fixed
+// 256-token blocks reached through the block table (same essay, Mountain 1;
+// nano-vllm hub page, "core tech 4").
+//
+// Design (GB300):
+//  * Work item = (sequence, kv head, logical block).  Items are equal-sized
+//    (one block of K and V for one head), so a persistent grid of
+//    (#SM x resident CTAs) walks them round-robin with no host sync; every CTA
+//    derives the item list itself from context_lens (block-wide scan in smem).
+//  * One producer warp streams the item's K tiles, then its V tiles, as 4-D
+//    TMA boxes {D, 1 head, 64 tokens, 1 block} into a ring of shared-memory
+//    stages; the block-table lookup is the box's outer coordinate.
+//  * Four consumer warps compute in fp32 on the CUDA cores (decode is
+//    HBM-bound: no GEMM reshaping).  All G = Hq/Hkv query heads of the group
+//    share each K/V tile read.  Phase 1: logits for the item's tokens (lane
+//    octets split D, a transposed shuffle reduction sums them).  Phase 2: exact
+//    softmax statistics of the item.  Phase 3: P.V with each lane owning D/32
+//    output dims.
+//  * Each item writes a partial (max, sum, unnormalised output) to the
+//    workspace; the last item of a (sequence, kv head) to finish (atomic
+//    ticket, no spinning) merges the partials and writes bf16.  A sequence
+//    that fits one block skips the workspace.
+#include <math.h>
+
+#include "host_common.h"
+#include "pkv_common.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kTile = 64;           // tokens per TMA tile
+constexpr int kConsumerWarps = 4;   // compute warps per CTA
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kStages = 3;          // shared-memory tile ring
+constexpr int kMaxSeqs = 16384;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct DecodeParams {
+  uint16_t *out;
+  const uint16_t *q;
+  const int32_t *block_tables;
+  const int32_t *context_lens;
+  int32_t *tickets;   // [num_seqs * Hkv]
+  float *part_ml;     // [max_total_blocks, Hq, 2]   (max in log2 units, sum)
+  float *part_o;      // [max_total_blocks, Hq, D]
+  int32_t *status;
+  int64_t num_blocks;
+  int64_t max_total_blocks;
+  int num_seqs;
+  int num_q_heads;
+  int num_kv_heads;
+  int block_size;
+  int max_blocks_per_seq;
+  float qscale;  // scale * log2(e)
+};
+
+__device__ __forceinline__ int named_bar_or(int id, int nthreads, int pred) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.s32 p, %3, 0;\n\t"
+      "bar.red.or.pred q, %1, %2, p;\n\t"
+      "selp.s32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(id), "r"(nthreads), "r"(pred)
+      : "memory");
+  return r;
+}
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// Blocks held by a sequence of context length L (clamped; *bad set on a bad L).
+__device__ __forceinline__ int seq_blocks(int L, int bs, int max_blocks, int *bad) {
+  if (L <= 0) {
+    *bad = 1;
+    return 0;
+  }
+  int nb = (L + bs - 1) / bs;
+  if (nb > max_blocks) {
+    *bad = 1;
+    nb = max_blocks;
+  }
+  return nb;
+}
+
+// Sum NV partial values over the 8 lanes of a lane octet (lane bits 0..2).
+// Transposed reduction: every xor step halves the live values.  Afterwards
+// lane r holds max(NV/8, 1) complete sums in v[0..): the values with original
+// index octet_base<NV>(r) + u.  For NV == 4, lanes r and r^1 hold the same sum.
+template <int NV>
+__device__ __forceinline__ void octet_reduce(float (&v)[NV], int r) {
+  static_assert(NV >= 4 && (NV & (NV - 1)) == 0, "NV must be a power of two >= 4");
+  constexpr int H1 = NV / 2;
+  {
+    const bool hi = (r & 4) != 0;
+#pragma unroll
+    for (int u = 0; u < H1; ++u) {
+      const float send = hi ? v[u] : v[u + H1];
+      const float keep = hi ? v[u + H1] : v[u];
+      v[u] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
+  }
+  constexpr int H2 = H1 / 2;
+  {
+    const bool hi = (r & 2) != 0;
+#pragma unroll
+    for (int u = 0; u < H2; ++u) {
+      const float send = hi ? v[u] : v[u + H2];
+      const float keep = hi ? v[u + H2] : v[u];
+      v[u] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+    }
+  }
+  if constexpr (H2 >= 2) {
+    constexpr int H3 = H2 / 2;
+    const bool hi = (r & 1) != 0;
+#pragma unroll
+    for (int u = 0; u < H3; ++u) {
+      const float send = hi ? v[u] : v[u + H3];
+      const float keep = hi ? v[u + H3] : v[u];
+      v[u] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+    }
+  } else {
+    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+  }
+}
+
+template <int NV>
+__device__ __forceinline__ int octet_base(int r) {
+  if constexpr (NV >= 8) {
+    return ((r & 4) ? NV / 2 : 0) + ((r & 2) ? NV / 4 : 0) + ((r & 1) ? NV / 8 : 0);
+  } else {
+    return ((r & 4) ? 2 : 0) + ((r & 2) ? 1 : 0);
+  }
+}
+
+template <int G>
+__device__ __forceinline__ void load_probs(const float *p, float (&pv)[G]) {
+  if constexpr (G == 1) {
+    pv[0] = p[0];
+  } else if constexpr (G == 2) {
+    const float2 a = *reinterpret_cast<const float2 *>(p);
+    pv[0] = a.x;
+    pv[1] = a.y;
+  } else {
+#pragma unroll
+    for (int i = 0; i < G; i += 4) {
+      const float4 a = *reinterpret_cast<const float4 *>(p + i);
+      pv[i] = a.x;
+      pv[i + 1] = a.y;
+      pv[i + 2] = a.z;
+      pv[i + 3] = a.w;
+    }
+  }
+}
+
+// Shared-memory carve-up (bytes), shared by host and device.
+struct DecodeSmem {
+  int tiles, bars, logits, red, stats, misc, prefix, total;
+  __host__ __device__ DecodeSmem(int D, int G, int bs, int num_seqs) {
+    tiles = 0;
+    bars = tiles + kStages * kTile * D * 2;
+    logits = bars + 2 * kStages * 8;
+    red = logits + ((bs * G * 4 + 15) & ~15);
+    stats = red + kConsumerWarps * G * D * 4;
+    misc = stats + 2 * G * 4;
+    prefix = misc + 16;
+    total = prefix + (num_seqs + 1) * 4;
+  }
+};
+
+template <int D, int G>
+__global__ void __launch_bounds__(kThreads)
+    paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
+  constexpr int kTileBytes = kTile * D * 2;
+  constexpr int CPL = D / 64;  // 16-byte chunks per lane per token (phase 1)
+  constexpr int DPL = D / 32;  // output dims per lane (phase 3)
+  constexpr int NV = 4 * G;    // partial dot products per lane (phase 1)
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const DecodeSmem lay(D, G, p.block_size, p.num_seqs);
+  uint8_t *tiles = smem + lay.tiles;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + lay.bars);
+  uint64_t *empty = full + kStages;
+  float *logits = reinterpret_cast<float *>(smem + lay.logits);  // [block_size][G]
+  float *red = reinterpret_cast<float *>(smem + lay.red);        // [warps][G][D]
+  float *mstat = reinterpret_cast<float *>(smem + lay.stats);    // [G]
+  float *lstat = mstat + G;                                      // [G]
+  int *misc = reinterpret_cast<int *>(smem + lay.misc);          // abort, last, total
+  int *prefix = reinterpret_cast<int *>(smem + lay.prefix);      // [num_seqs + 1]
+  volatile int *abort_flag = misc;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int S = p.num_seqs;
+  const int BS = p.block_size;
+  const int Hkv = p.num_kv_heads;
+  const int Hq = p.num_q_heads;
+
+  // ---- prologue: barriers, and the block prefix over sequences -----------
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kConsumerWarps);
+    }
+    misc[0] = 0;
+    misc[1] = 0;
+    fence_barrier_init();
+  }
+  if (tid == kConsumerWarps * 32) {
+    tma_prefetch_map(&tm_k);
+    tma_prefetch_map(&tm_v);
+  }
+  const int per = (S + kThreads - 1) / kThreads;
+  const int s_begin = min(tid * per, S);
+  const int s_end = min(s_begin + per, S);
+  int bad = 0;
+  int local = 0;
+  for (int s = s_begin; s < s_end; ++s)
+    local += seq_blocks(p.context_lens[s], BS, p.max_blocks_per_seq, &bad);
+  if (bad && blockIdx.x == 0) flag_status(p.status, PKV_DEV_BAD_CONTEXT);
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  // Warp totals go to the (still unused) reduction area.
+  if (lane == 31) red[warp] = __int_as_float(incl);
+  __syncthreads();
+  int offset = incl - local;
+  int total = 0;
+  for (int w = 0; w < kThreads / 32; ++w) {
+    const int wt = __float_as_int(red[w]);
+    if (w < warp) offset += wt;
+    total += wt;
+  }
+  {
+    int run = offset;
+    int dummy = 0;
+    for (int s = s_begin; s < s_end; ++s) {
+      prefix[s] = run;
+      run += seq_blocks(p.context_lens[s], BS, p.max_blocks_per_seq, &dummy);
+    }
+    if (tid == 0) prefix[S] = total;
+  }
+  __syncthreads();
+  if ((int64_t)total > p.max_total_blocks) {
+    if (blockIdx.x == 0 && tid == 0) flag_status(p.status, PKV_DEV_WORKSPACE);
+    return;
+  }
+  const int total_items = total * Hkv;
+
+  auto item_coords = [&](int w, int &s, int &b, int &j, int &gblk) {
+    gblk = w / Hkv;
+    j = w - gblk * Hkv;
+    int lo = 0, hi = S - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (prefix[mid] <= gblk)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    s = lo;
+    b = gblk - prefix[s];
+  };
+
+  // ---- producer warp: TMA K tiles then V tiles of every item ---------------
+  if (warp == kConsumerWarps) {
+    if (lane == 0) {
+      const uint64_t policy = l2_policy_evict_first();
+      int issued = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; w < total_items && ok; w += gridDim.x) {
+        int s, b, j, gblk;
+        item_coords(w, s, b, j, gblk);
+        const int L = min(p.context_lens[s], p.max_blocks_per_seq * BS);
+        const int valid = min(BS, L - b * BS);
+        const int ntile = (valid + kTile - 1) / kTile;
+        int blk = p.block_tables[(int64_t)s * p.max_blocks_per_seq + b];
+        if (blk < 0 || (int64_t)blk >= p.num_blocks) {
+          flag_status(p.status, PKV_DEV_BAD_BLOCK);
+          blk = 0;
+        }
+        for (int half = 0; half < 2 && ok; ++half) {
+          const CUtensorMap *map = half ? &tm_v : &tm_k;
+          for (int t = 0; t < ntile; ++t) {
+            const int st = issued % kStages;
+            if (issued >= kStages &&
+                !mbar_wait_bounded(&empty[st], ((issued / kStages) - 1) & 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&full[st], kTileBytes);
+            tma_load_4d_hint(tiles + st * kTileBytes, map, &full[st], 0, j, t * kTile, blk,
+                             policy);
+            ++issued;
+          }
+        }
+      }
+      if (!ok) flag_status(p.status, PKV_DEV_TIMEOUT);
+      // Do not leave while copies into this CTA's shared memory are in flight.
+      for (int i = max(0, issued - kStages); i < issued; ++i)
+        mbar_wait_bounded(&full[i % kStages], (i / kStages) & 1, nullptr);
+    }
+    return;
+  }
+
+  // ---- consumer warps -----------------------------------------------------
+  const int r = lane & 7;     // lane within its octet
+  const int gid = lane >> 3;  // octet index: 4 tokens each
+  int ctile = 0;              // tiles consumed so far
+  for (int w = blockIdx.x; w < total_items; w += gridDim.x) {
+    int s, b, j, gblk;
+    item_coords(w, s, b, j, gblk);
+    const int L = min(p.context_lens[s], p.max_blocks_per_seq * BS);
+    const int valid = min(BS, L - b * BS);
+    const int ntile = (valid + kTile - 1) / kTile;
+    const int nblk = prefix[s + 1] - prefix[s];
+    const int h0 = j * G;
+
+    // q fragment: dims of chunks r + 8c, pre-scaled into log2 units.
+    float qf[G][CPL * 8];
+    {
+      const uint16_t *qrow = p.q + ((int64_t)s * Hq + h0) * D;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+          const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(qrow + h * D + (r + 8 * c) * 8));
+          const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            qf[h][c * 8 + 2 * e] = bf16lo(wv[e]) * p.qscale;
+            qf[h][c * 8 + 2 * e + 1] = bf16hi(wv[e]) * p.qscale;
+          }
+        }
+      }
+    }
+
+    // Phase 1: logits of the item's tokens.
+    for (int t = 0; t < ntile; ++t, ++ctile) {
+      const int st = ctile % kStages;
+      const bool ok = mbar_wait_bounded(&full[st], (ctile / kStages) & 1, abort_flag);
+      if (ok) {
+        const uint16_t *tile = reinterpret_cast<const uint16_t *>(tiles + st * kTileBytes);
+        const int tok0 = warp * 16 + gid * 4;
+        float acc[NV];
+#pragma unroll
+        for (int i = 0; i < NV; ++i) acc[i] = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint16_t *krow = tile + (tok0 + i) * D;
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) {
+            const uint4 raw = *reinterpret_cast<const uint4 *>(krow + (r + 8 * c) * 8);
+            const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float k0 = bf16lo(wv[e]);
+              const float k1 = bf16hi(wv[e]);
+#pragma unroll
+              for (int h = 0; h < G; ++h) {
+                acc[i * G + h] = fmaf(qf[h][c * 8 + 2 * e], k0, acc[i * G + h]);
+                acc[i * G + h] = fmaf(qf[h][c * 8 + 2 * e + 1], k1, acc[i * G + h]);
+              }
+            }
+          }
+        }
+        octet_reduce<NV>(acc, r);
+        const int base = octet_base<NV>(r);
+        constexpr int kOwned = NV >= 8 ? NV / 8 : 1;
+        if (NV >= 8 || (r & 1) == 0) {
+#pragma unroll
+          for (int u = 0; u < kOwned; ++u) {
+            const int vi = base + u;
+            const int i = vi / G;
+            const int h = vi - i * G;
+            logits[(t * kTile + tok0 + i) * G + h] = acc[u];
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+    }
+    named_bar_sync(1, kConsumerWarps * 32);
+
+    // Phase 2: exact softmax statistics of this item, per head.
+    for (int h = warp; h < G; h += kConsumerWarps) {
+      float m = -INFINITY;
+      for (int x = lane; x < valid; x += 32) m = fmaxf(m, logits[x * G + h]);
+      m = warp_max(m);
+      float l = 0.f;
+      for (int x = lane; x < valid; x += 32) {
+        const float e = fast_exp2(logits[x * G + h] - m);
+        logits[x * G + h] = e;
+        l += e;
+      }
+      l = warp_sum(l);
+      if (lane == 0) {
+        mstat[h] = m;
+        lstat[h] = l;
+      }
+    }
+    named_bar_sync(1, kConsumerWarps * 32);
+
+    // Phase 3: unnormalised P.V, lane owns dims [lane*DPL, lane*DPL + DPL).
+    float acc_o[G][DPL];
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) acc_o[h][e] = 0.f;
+    for (int t = 0; t < ntile; ++t, ++ctile) {
+      const int st = ctile % kStages;
+      const bool ok = mbar_wait_bounded(&full[st], (ctile / kStages) & 1, abort_flag);
+      if (ok) {
+        const uint16_t *tile = reinterpret_cast<const uint16_t *>(tiles + st * kTileBytes);
+        const int tlo = warp * 16;
+        const int thi = min(tlo + 16, valid - t * kTile);
+#pragma unroll 4
+        for (int tok = tlo; tok < thi; ++tok) {
+          float vf[DPL];
+          if constexpr (DPL == 4) {
+            const uint2 raw = *reinterpret_cast<const uint2 *>(tile + tok * D + lane * 4);
+            vf[0] = bf16lo(raw.x);
+            vf[1] = bf16hi(raw.x);
+            vf[2] = bf16lo(raw.y);
+            vf[3] = bf16hi(raw.y);
+          } else {
+            const uint32_t raw = *reinterpret_cast<const uint32_t *>(tile + tok * D + lane * 2);
+            vf[0] = bf16lo(raw);
+            vf[1] = bf16hi(raw);
+          }
+          float pv[G];
+          load_probs<G>(logits + (t * kTile + tok) * G, pv);
+#pragma unroll
+          for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) acc_o[h][e] = fmaf(pv[h], vf[e], acc_o[h][e]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+    }
+
+    // Epilogue: combine the four warps, then finish or publish a partial.
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) red[(warp * G + h) * D + lane * DPL + e] = acc_o[h][e];
+    named_bar_sync(1, kConsumerWarps * 32);
+    if (nblk == 1) {
+      for (int idx = tid; idx < G * D / 2; idx += kConsumerWarps * 32) {
+        const int e = idx * 2;
+        const int h = e / D;
+        float o0 = 0.f, o1 = 0.f;
+#pragma unroll
+        for (int q = 0; q < kConsumerWarps; ++q) {
+          o0 += red[q * G * D + e];
+          o1 += red[q * G * D + e + 1];
+        }
+        const float inv = 1.f / lstat[h];
+        *reinterpret_cast<uint32_t *>(p.out + ((int64_t)s * Hq + h0) * D + e) =
+            pack_bf16x2(o0 * inv, o1 * inv);
+      }
+    } else {
+      float *po = p.part_o + ((int64_t)gblk * Hq + h0) * D;
+      for (int idx = tid; idx < G * D / 4; idx += kConsumerWarps * 32) {
+        const int e = idx * 4;
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < kConsumerWarps; ++q) {
+          const float4 x = *reinterpret_cast<const float4 *>(red + q * G * D + e);
+          o.x += x.x;
+          o.y += x.y;
+          o.z += x.z;
+          o.w += x.w;
+        }
+        *reinterpret_cast<float4 *>(po + e) = o;
+      }
+      if (tid < G) {
+        p.part_ml[((int64_t)gblk * Hq + h0 + tid) * 2] = mstat[tid];
+        p.part_ml[((int64_t)gblk * Hq + h0 + tid) * 2 + 1] = lstat[tid];
+      }
+      __threadfence();
+      named_bar_sync(1, kConsumerWarps * 32);
+      if (tid == 0) {
+        const unsigned old =
+            atomicInc(reinterpret_cast<unsigned *>(p.tickets + (int64_t)s * Hkv + j),
+                      (unsigned)(nblk - 1));
+        misc[1] = (old == (unsigned)(nblk - 1)) ? 1 : 0;
+      }
+      named_bar_sync(1, kConsumerWarps * 32);
+      if (misc[1]) {
+        // Last partial of (s, j): merge all nblk partials.
+        __threadfence();
+        const int pb0 = prefix[s];
+        for (int h = warp; h < G; h += kConsumerWarps) {
+          float M = -INFINITY;
+          for (int bb = lane; bb < nblk; bb += 32)
+            M = fmaxf(M, __ldcg(p.part_ml + ((int64_t)(pb0 + bb) * Hq + h0 + h) * 2));
+          M = warp_max(M);
+          float Ls = 0.f;
+          for (int bb = lane; bb < nblk; bb += 32) {
+            const float *ml = p.part_ml + ((int64_t)(pb0 + bb) * Hq + h0 + h) * 2;
+            Ls += fast_exp2(__ldcg(ml) - M) * __ldcg(ml + 1);
+          }
+          Ls = warp_sum(Ls);
+          if (lane == 0) {
+            mstat[h] = M;
+            lstat[h] = 1.f / Ls;
+          }
+        }
+        named_bar_sync(1, kConsumerWarps * 32);
+        for (int idx = tid; idx < G * D / 4; idx += kConsumerWarps * 32) {
+          const int e = idx * 4;
+          const int h = e / D;
+          const float M = mstat[h];
+          float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+          for (int bb = 0; bb < nblk; ++bb) {
+            const int64_t row = (int64_t)(pb0 + bb) * Hq + h0 + h;
+            const float wgt = fast_exp2(__ldcg(p.part_ml + row * 2) - M);
+            const float4 x = __ldcg(reinterpret_cast<const float4 *>(p.part_o + row * D + e - h * D));
+            o.x = fmaf(wgt, x.x, o.x);
+            o.y = fmaf(wgt, x.y, o.y);
+            o.z = fmaf(wgt, x.z, o.z);
+            o.w = fmaf(wgt, x.w, o.w);
+          }
+          const float inv = lstat[h];
+          uint16_t *dst = p.out + ((int64_t)s * Hq + h0) * D + e;
+          uint2 packed;
+          packed.x = pack_bf16x2(o.x * inv, o.y * inv);
+          packed.y = pack_bf16x2(o.z * inv, o.w * inv);
+          *reinterpret_cast<uint2 *>(dst) = packed;
+        }
+      }
+    }
+    // All consumer warps agree on whether to stop (a wait ran out).
+    if (named_bar_or(1, kConsumerWarps * 32, *abort_flag != 0)) {
+      if (tid == 0) flag_status(p.status, PKV_DEV_TIMEOUT);
+      break;
+    }
+  }
+}
+
+template <int D, int G>
+pkv_status launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &prm,
+                         int64_t max_items, cudaStream_t stream) {
+  const DecodeSmem lay(D, G, prm.block_size, prm.num_seqs);
+  const int smem = lay.total + 1024;  // + alignment slack
+  static int configured_smem = 0;
+  static int ctas_per_sm = 0;
+  if (configured_smem < smem) {
+    if (cudaFuncSetAttribute(paged_decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    configured_smem = smem;
+    ctas_per_sm = 0;
+  }
+  static int occ_smem = -1;
+  if (occ_smem != smem || ctas_per_sm == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, paged_decode_kernel<D, G>, kThreads,
+                                                      smem) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    ctas_per_sm = n > 0 ? n : 1;
+    occ_smem = smem;
+  }
+  const int sms = device_sm_count();
+  if (sms <= 0) return PKV_ERR_CUDA;
+  int64_t grid = (int64_t)sms * ctas_per_sm;
+  if (grid > max_items) grid = max_items;
+  if (grid < 1) grid = 1;
+  paged_decode_kernel<D, G><<<(unsigned)grid, kThreads, smem, stream>>>(tk, tv, prm);
+  return launch_status();
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
+                                            int head_dim, int64_t max_total_blocks) {
+  using pkv::align256;
+  if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+      max_total_blocks < 0)
+    return 0;
+  return align256((size_t)num_seqs * num_kv_heads * 4) +
+         align256((size_t)max_total_blocks * num_q_heads * 2 * 4) +
+         align256((size_t)max_total_blocks * num_q_heads * head_dim * 4);
+}
+
+extern "C" pkv_status pkv_paged_decode_attn(uint16_t *out, const uint16_t *q,
+                                            const uint16_t *k_cache, const uint16_t *v_cache,
+                                            const int32_t *block_tables,
+                                            const int32_t *context_lens, int num_seqs,
+                                            int num_q_heads, int num_kv_heads, int head_dim,
+                                            int block_size, int max_blocks_per_seq,
+                                            int64_t num_blocks, int64_t max_total_blocks,
+                                            float scale, void *workspace, size_t workspace_bytes,
+                                            int32_t *dev_status, void *stream) {
+  using namespace pkv;
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+      block_size <= 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 || max_total_blocks < 0)
+    return PKV_ERR_INVALID_ARG;
+  if (num_q_heads % num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+  const int G = num_q_heads / num_kv_heads;
+  if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return PKV_ERR_UNSUPPORTED;
+  if (block_size != 64 && block_size != 128 && block_size != 256 && block_size != 512)
+    return PKV_ERR_UNSUPPORTED;
+  if (num_seqs > kMaxSeqs) return PKV_ERR_UNSUPPORTED;
+  if (!(scale == scale)) return PKV_ERR_INVALID_ARG;
+  if (num_seqs == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PKV_ERR_INVALID_ARG;
+  const size_t need =
+      pkv_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_total_blocks);
+  if (workspace == nullptr || workspace_bytes < need ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return PKV_ERR_WORKSPACE;
+
+  DecodeParams prm;
+  prm.out = out;
+  prm.q = q;
+  prm.block_tables = block_tables;
+  prm.context_lens = context_lens;
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  prm.tickets = reinterpret_cast<int32_t *>(ws);
+  ws += align256((size_t)num_seqs * num_kv_heads * 4);
+  prm.part_ml = reinterpret_cast<float *>(ws);
+  ws += align256((size_t)max_total_blocks * num_q_heads * 2 * 4);
+  prm.part_o = reinterpret_cast<float *>(ws);
+  prm.status = dev_status;
+  prm.num_blocks = num_blocks;
+  prm.max_total_blocks = max_total_blocks;
+  prm.num_seqs = num_seqs;
+  prm.num_q_heads = num_q_heads;
+  prm.num_kv_heads = num_kv_heads;
+  prm.block_size = block_size;
+  prm.max_blocks_per_seq = max_blocks_per_seq;
+  prm.qscale = scale * kLog2e;
+
+  // K/V cache as a 4-D tensor {D, Hkv, block_size, num_blocks}; a box is one
+  // kv head's 64 consecutive tokens of one block.
+  const uint64_t dims[4] = {(uint64_t)head_dim, (uint64_t)num_kv_heads, (uint64_t)block_size,
+                            (uint64_t)num_blocks};
+  const uint64_t strides[3] = {(uint64_t)head_dim * 2, (uint64_t)num_kv_heads * head_dim * 2,
+                               (uint64_t)block_size * num_kv_heads * head_dim * 2};
+  const uint32_t box[4] = {(uint32_t)head_dim, 1u, (uint32_t)kTile, 1u};
+  CUtensorMap tk, tv;
+  if (!encode_bf16_map(&tk, k_cache, 4, dims, strides, box, false) ||
+      !encode_bf16_map(&tv, v_cache, 4, dims, strides, box, false))
+    return PKV_ERR_CUDA;
+
+  int64_t max_items = (int64_t)num_seqs * max_blocks_per_seq;
+  if (max_items > max_total_blocks) max_items = max_total_blocks;
+  max_items *= num_kv_heads;
+  if (max_items < 1) max_items = 1;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+#define PKV_DECODE_CASE(DD, GG) \
+  if (head_dim == DD && G == GG) return launch_decode<DD, GG>(tk, tv, prm, max_items, st);
+  PKV_DECODE_CASE(64, 1)
+  PKV_DECODE_CASE(64, 2)
+  PKV_DECODE_CASE(64, 4)
+  PKV_DECODE_CASE(64, 8)
+  PKV_DECODE_CASE(128, 1)
+  PKV_DECODE_CASE(128, 2)
+  PKV_DECODE_CASE(128, 4)
+  PKV_DECODE_CASE(128, 8)
+#undef PKV_DECODE_CASE
+  return PKV_ERR_UNSUPPORTED;
+}

@@ -1,0 +1,501 @@
+// prefill.cu -- causal varlen prefill attention over the paged cache (tcgen05).
+//
+// Prefill processes whole prompts at once and is compute-dense, unlike decode
+// (CSDN essay "from nanoVLLM to vLLM", Mountain 3 and the study route's note
+// on the attention/ module).  Its keys and values, including a prefix that was
+// cached earlier, live in fixed 256-token blocks reached through the block
+// table (same essay, Mountain 1; nano-vllm hub page, "core tech 4").  The
+// result is standard softmax attention; like FlashAttention the kernel only
+// reorders the computation into on-chip tiles (same essay, Mountain 3).
+//
+// Design (GB300):
+//  * One CTA per (sequence, 128-query tile, pair of query heads of one GQA
+//    group); CTAs are ordered heaviest-tile-first.  The two heads share every
+//    K/V tile.
+//  * Warp 0 issues TMA: the Q tiles once, then K and V tiles of 64 keys as
+//    128B-swizzled 4-D boxes {64 dims, 1 head, 64 tokens, 1 block}, the block
+//    id coming from the block table, into a 2-stage ring.
+//  * Warp 1 issues tcgen05.mma: S_h = Q_h K^T (M=128, N=64) into tensor memory,
+//    then O_h += P_h V (M=128, N=D) with V as an MN-major operand.
+//  * Warps 2-5 (one thread per query row) read S from tensor memory, apply the
+//    causal mask offset by the cached length, run the online softmax in fp32
+//    (log2 domain), rescale O in tensor memory when the row max grows, write
+//    P as bf16 into shared memory in the MMA's swizzled layout, and finally
+//    normalise O and store bf16 rows.
+#include <math.h>
+
+#include "host_common.h"
+#include "pkv_common.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int BM = 128;  // query rows per tile (MMA M)
+constexpr int BN = 64;   // keys per tile
+constexpr int kStages = 2;
+constexpr int kThreads = 192;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct PrefillParams {
+  uint16_t *out;
+  const int32_t *block_tables;
+  const int32_t *cu_q;
+  const int32_t *cu_k;
+  int32_t *status;
+  int64_t num_blocks;
+  int64_t total_q;
+  int num_seqs;
+  int num_q_heads;
+  int num_kv_heads;
+  int block_size;
+  int max_blocks_per_seq;
+  int q_tiles;  // ceil(max_seqlen_q / BM)
+  float qscale; // scale * log2(e)
+};
+
+template <int D, int NH>
+struct PrefillLayout {
+  static constexpr int kQBytes = BM * D * 2;   // one head's Q tile
+  static constexpr int kKVBytes = BN * D * 2;  // one K or V tile
+  static constexpr int kPBytes = BM * BN * 2;  // one head's P tile
+  static constexpr int q = 0;
+  static constexpr int k = q + NH * kQBytes;
+  static constexpr int v = k + kStages * kKVBytes;
+  static constexpr int p = v + kStages * kKVBytes;
+  static constexpr int bars = p + NH * kPBytes;
+  // barriers: q_full, k_full[S], v_full[S], kv_empty[S], s_full[NH], p_full[NH], o_done[NH], drain
+  static constexpr int kNumBars = 1 + 3 * kStages + 3 * NH + 1;
+  static constexpr int misc = bars + kNumBars * 8;  // tmem address, abort flag
+  static constexpr int total = misc + 16;
+  static constexpr int kTmemCols = NH * (BN + D) <= 128 ? 128 : (NH * (BN + D) <= 256 ? 256 : 512);
+};
+
+// Tensor-memory columns: O_h at kOCol + h*D, S_h at kSCol + h*BN (fp32, lane = row).
+template <int D, int NH>
+struct TmemCols {
+  static constexpr uint32_t kO = 0;
+  static constexpr uint32_t kS = NH * D;
+};
+
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+  const bool ok = mbar_wait_bounded(bar, parity, abort);
+  return __all_sync(0xffffffffu, ok);
+}
+
+template <int D, int NH>
+__global__ void __launch_bounds__(kThreads, 1)
+    paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
+                         const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
+  using L = PrefillLayout<D, NH>;
+  constexpr int XR = D / 64;  // 128-byte swizzle regions across D
+  constexpr uint32_t kOCol = TmemCols<D, NH>::kO;
+  constexpr uint32_t kSCol = TmemCols<D, NH>::kS;
+
+  // ---- which tile -------------------------------------------------------
+  const int HG = p.num_q_heads / NH;
+  int idx = blockIdx.x;
+  const int hg = idx % HG;
+  idx /= HG;
+  const int s = idx % p.num_seqs;
+  const int tr = idx / p.num_seqs;  // 0 = the sequence's last (heaviest) q tile
+  const int q_begin = p.cu_q[s];
+  const int n = p.cu_q[s + 1] - q_begin;
+  const int len_k = p.cu_k[s + 1] - p.cu_k[s];
+  const int c = len_k - n;
+  if (n <= 0) return;
+  const int ntq = (n + BM - 1) / BM;
+  if (c < 0 || len_k > p.max_blocks_per_seq * p.block_size || ntq > p.q_tiles ||
+      (int64_t)q_begin + n > p.total_q) {
+    if (tr == 0 && hg == 0 && threadIdx.x == 0) flag_status(p.status, PKV_DEV_BAD_SEQLEN);
+    if (c < 0 || len_k > p.max_blocks_per_seq * p.block_size || (int64_t)q_begin + n > p.total_q)
+      return;
+  }
+  const int t = ntq - 1 - tr;
+  if (t < 0) return;
+  const int q0 = t * BM;
+  const int rows_valid = min(BM, n - q0);
+  const int kv_end = min(len_k, c + q0 + rows_valid);  // keys needed by this tile
+  const int n_kv = (kv_end + BN - 1) / BN;
+  const int h_first = hg * NH;
+  const int G = p.num_q_heads / p.num_kv_heads;
+  const int kvh = h_first / G;
+
+  // ---- shared memory ----------------------------------------------------
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t *sQ = smem + L::q;
+  uint8_t *sK = smem + L::k;
+  uint8_t *sV = smem + L::v;
+  uint8_t *sP = smem + L::p;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::bars);
+  uint64_t *q_full = bars;
+  uint64_t *k_full = bars + 1;
+  uint64_t *v_full = k_full + kStages;
+  uint64_t *kv_empty = v_full + kStages;
+  uint64_t *s_full = kv_empty + kStages;
+  uint64_t *p_full = s_full + NH;
+  uint64_t *o_done = p_full + NH;
+  uint64_t *drain = o_done + NH;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::misc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::misc + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+    }
+    for (int h = 0; h < NH; ++h) {
+      mbar_init(&s_full[h], 1);
+      mbar_init(&p_full[h], 128);
+      mbar_init(&o_done[h], 1);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, L::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ================= TMA producer =================
+    if (lane == 0) {
+      tma_prefetch_map(&tm_q);
+      tma_prefetch_map(&tm_k);
+      tma_prefetch_map(&tm_v);
+      mbar_arrive_expect_tx(q_full, NH * L::kQBytes);
+      for (int h = 0; h < NH; ++h)
+        for (int x = 0; x < XR; ++x)
+          tma_load_3d(sQ + h * L::kQBytes + x * BM * 128, &tm_q, q_full, x * 64, h_first + h,
+                      q_begin + q0);
+      int issued = 0;
+      for (int jt = 0; jt < n_kv; ++jt) {
+        const int st = jt % kStages;
+        if (jt >= kStages &&
+            !mbar_wait_bounded(&kv_empty[st], ((jt / kStages) - 1) & 1, abort_flag))
+          break;
+        const int key0 = jt * BN;
+        const int lb = key0 / p.block_size;
+        const int off = key0 - lb * p.block_size;
+        int blk = p.block_tables[(int64_t)s * p.max_blocks_per_seq + lb];
+        if (blk < 0 || (int64_t)blk >= p.num_blocks) {
+          flag_status(p.status, PKV_DEV_BAD_BLOCK);
+          blk = 0;
+        }
+        mbar_arrive_expect_tx(&k_full[st], L::kKVBytes);
+        for (int x = 0; x < XR; ++x)
+          tma_load_4d(sK + st * L::kKVBytes + x * BN * 128, &tm_k, &k_full[st], x * 64, kvh, off,
+                      blk);
+        mbar_arrive_expect_tx(&v_full[st], L::kKVBytes);
+        for (int x = 0; x < XR; ++x)
+          tma_load_4d(sV + st * L::kKVBytes + x * BN * 128, &tm_v, &v_full[st], x * 64, kvh, off,
+                      blk);
+        issued = jt + 1;
+      }
+      // Do not leave while copies into this CTA's shared memory are in flight.
+      mbar_wait_bounded(q_full, 0, nullptr);
+      for (int i = max(0, issued - kStages); i < issued; ++i) {
+        mbar_wait_bounded(&k_full[i % kStages], (i / kStages) & 1, nullptr);
+        mbar_wait_bounded(&v_full[i % kStages], (i / kStages) & 1, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    // ================= MMA issuer =================
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = umma_idesc_bf16(BM, BN, false, false);
+      constexpr uint32_t idesc_o = umma_idesc_bf16(BM, D, false, true);
+      const uint32_t q_addr = smem_u32(sQ);
+      const uint32_t k_addr = smem_u32(sK);
+      const uint32_t v_addr = smem_u32(sV);
+      const uint32_t p_addr = smem_u32(sP);
+      bool ok = mbar_wait_bounded(q_full, 0, abort_flag);
+      tc_fence_after_sync();
+      auto issue_pv = [&](int jt, int h) {
+        const int pst = jt % kStages;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          const uint64_t a = umma_desc_sw128(p_addr + h * L::kPBytes + kk * 32, 16, 1024);
+          const uint64_t b =
+              umma_desc_sw128(v_addr + pst * L::kKVBytes + kk * 16 * 128, BN * 128, 1024);
+          umma_bf16(tmem + kOCol + h * D, a, b, idesc_o, (jt > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(&o_done[h]);
+      };
+      for (int jt = 0; jt < n_kv && ok; ++jt) {
+        const int st = jt % kStages;
+        ok = mbar_wait_bounded(&k_full[st], (jt / kStages) & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after_sync();
+        for (int h = 0; h < NH && ok; ++h) {
+          if (jt > 0) {
+            ok = mbar_wait_bounded(&p_full[h], (jt - 1) & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after_sync();
+          }
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk & 3) * 32;
+            const uint64_t a =
+                umma_desc_sw128(q_addr + h * L::kQBytes + (kk / 4) * BM * 128 + off, 16, 1024);
+            const uint64_t b =
+                umma_desc_sw128(k_addr + st * L::kKVBytes + (kk / 4) * BN * 128 + off, 16, 1024);
+            umma_bf16(tmem + kSCol + h * BN, a, b, idesc_s, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(&s_full[h]);
+          if (jt > 0) {
+            if (h == 0) {
+              ok = mbar_wait_bounded(&v_full[(jt - 1) % kStages], ((jt - 1) / kStages) & 1,
+                                     abort_flag);
+              if (!ok) break;
+              tc_fence_after_sync();
+            }
+            issue_pv(jt - 1, h);
+          }
+        }
+        if (ok && jt > 0) umma_commit(&kv_empty[(jt - 1) % kStages]);
+      }
+      if (ok) {
+        const int last = n_kv - 1;
+        ok = mbar_wait_bounded(&v_full[last % kStages], (last / kStages) & 1, abort_flag);
+        for (int h = 0; h < NH && ok; ++h) {
+          ok = mbar_wait_bounded(&p_full[h], last & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after_sync();
+          issue_pv(last, h);
+        }
+      }
+      // Wait for every MMA this thread issued before tensor memory is freed.
+      umma_commit(drain);
+      mbar_wait_bounded(drain, 0, nullptr);
+    }
+  } else {
+    // ================= softmax / epilogue warpgroup =================
+    const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    const int key_limit = min(c + q0 + row, len_k - 1);  // last key this row may see
+    float m_run[NH], l_run[NH];
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+      m_run[h] = -INFINITY;
+      l_run[h] = 0.f;
+    }
+    bool ok = true;
+    for (int jt = 0; jt < n_kv && ok; ++jt) {
+      const int key0 = jt * BN;
+      for (int h = 0; h < NH && ok; ++h) {
+        ok = warp_wait(&s_full[h], jt & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after_sync();
+        float sv[BN / 32][32];
+#pragma unroll
+        for (int hh = 0; hh < BN / 32; ++hh)
+          tmem_load32(tmem + lane_base + kSCol + h * BN + hh * 32, sv[hh]);
+        float mt = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < BN; ++i) {
+          const float x = (key0 + i <= key_limit) ? sv[i / 32][i % 32] * p.qscale : -INFINITY;
+          sv[i / 32][i % 32] = x;
+          mt = fmaxf(mt, x);
+        }
+        const float m_new = fmaxf(m_run[h], mt);
+        const float alpha = fast_exp2(m_run[h] - m_new);
+        float rs = 0.f;
+#pragma unroll
+        for (int i = 0; i < BN; ++i) {
+          sv[i / 32][i % 32] = fast_exp2(sv[i / 32][i % 32] - m_new);
+          rs += sv[i / 32][i % 32];
+        }
+        if (jt > 0) {
+          // PV of the previous tile must be complete: O is rescaled, P reused.
+          ok = warp_wait(&o_done[h], (jt - 1) & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after_sync();
+          if (__any_sync(0xffffffffu, alpha < 1.f)) {
+#pragma unroll 1
+            for (int cc = 0; cc < D / 32; ++cc) {
+              float ov[32];
+              const uint32_t oa = tmem + lane_base + kOCol + h * D + cc * 32;
+              tmem_load32(oa, ov);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) ov[i] *= alpha;
+              tmem_store32(oa, ov);
+            }
+          }
+        }
+        l_run[h] = l_run[h] * alpha + rs;
+        m_run[h] = m_new;
+        if (h == 0 && jt == n_kv - 1 && key0 + BN > len_k) {
+          // Keys past the context may hold stale bits (even NaN); P is zero
+          // there, but 0 * NaN is not, so clear those V rows first.
+          ok = warp_wait(&v_full[jt % kStages], (jt / kStages) & 1, abort_flag);
+          if (!ok) break;
+          const int first = len_k - key0;
+          uint8_t *vt = sV + (jt % kStages) * L::kKVBytes;
+          const int nchunks = (BN - first) * 8 * XR;  // 16-byte chunks to clear
+          for (int i = row; i < nchunks; i += 128) {
+            const int x = i / ((BN - first) * 8);
+            const int rem = i - x * (BN - first) * 8;
+            const int rr = first + rem / 8;
+            *reinterpret_cast<uint4 *>(vt + x * BN * 128 + rr * 128 + (rem & 7) * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+        }
+        // P (bf16) into the 128B-swizzled K-major tile: row `row`, 16-byte chunk c
+        // of keys 8c..8c+7 lands at chunk c ^ (row & 7).
+        uint8_t *prow = sP + h * L::kPBytes + row * 128;
+#pragma unroll
+        for (int cidx = 0; cidx < BN / 8; ++cidx) {
+          uint4 w;
+          const float *pv = &sv[cidx / 4][(cidx % 4) * 8];
+          w.x = pack_bf16x2(pv[0], pv[1]);
+          w.y = pack_bf16x2(pv[2], pv[3]);
+          w.z = pack_bf16x2(pv[4], pv[5]);
+          w.w = pack_bf16x2(pv[6], pv[7]);
+          *reinterpret_cast<uint4 *>(prow + ((cidx ^ (row & 7)) * 16)) = w;
+        }
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        mbar_arrive(&p_full[h]);
+      }
+    }
+    // Epilogue: O / l -> bf16 rows.
+    for (int h = 0; h < NH && ok; ++h) {
+      ok = warp_wait(&o_done[h], (n_kv - 1) & 1, abort_flag);
+      if (!ok) break;
+      tc_fence_after_sync();
+      const float inv = 1.f / l_run[h];
+      uint16_t *dst = p.out + ((int64_t)(q_begin + q0 + row) * p.num_q_heads + h_first + h) * D;
+#pragma unroll 1
+      for (int cc = 0; cc < D / 32; ++cc) {
+        float ov[32];
+        tmem_load32(tmem + lane_base + kOCol + h * D + cc * 32, ov);
+        if (row < rows_valid) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            uint4 w;
+            w.x = pack_bf16x2(ov[i] * inv, ov[i + 1] * inv);
+            w.y = pack_bf16x2(ov[i + 2] * inv, ov[i + 3] * inv);
+            w.z = pack_bf16x2(ov[i + 4] * inv, ov[i + 5] * inv);
+            w.w = pack_bf16x2(ov[i + 6] * inv, ov[i + 7] * inv);
+            *reinterpret_cast<uint4 *>(dst + cc * 32 + i) = w;
+          }
+        }
+      }
+    }
+    tc_fence_before_sync();
+  }
+
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_flag) flag_status(p.status, PKV_DEV_TIMEOUT);
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, L::kTmemCols);
+  }
+}
+
+template <int D, int NH>
+pkv_status launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                          const PrefillParams &prm, cudaStream_t stream) {
+  using L = PrefillLayout<D, NH>;
+  static int smem = 0;
+  if (smem == 0) {
+    int bytes = L::total + 1024;
+    // Resident CTAs per SM must not ask for more than 512 TMEM columns in
+    // total, or tcgen05.alloc would stall: pad shared memory to cap occupancy.
+    const int max_ctas = 512 / L::kTmemCols;
+    const int per_sm = 228 * 1024;
+    const int min_bytes = per_sm / (max_ctas + 1) + 1;
+    if (bytes < min_bytes) bytes = min_bytes;
+    if (cudaFuncSetAttribute(paged_prefill_kernel<D, NH>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    smem = bytes;
+  }
+  const int64_t grid = (int64_t)prm.q_tiles * prm.num_seqs * (prm.num_q_heads / NH);
+  if (grid > 0x7FFFFFFFLL) return PKV_ERR_INVALID_ARG;
+  paged_prefill_kernel<D, NH><<<(unsigned)grid, kThreads, smem, stream>>>(tq, tk, tv, prm);
+  return launch_status();
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" pkv_status pkv_paged_prefill_attn(uint16_t *out, const uint16_t *q,
+                                             const uint16_t *k_cache, const uint16_t *v_cache,
+                                             const int32_t *block_tables,
+                                             const int32_t *cu_seqlens_q,
+                                             const int32_t *cu_seqlens_k, int num_seqs,
+                                             int64_t total_q, int max_seqlen_q, int num_q_heads,
+                                             int num_kv_heads, int head_dim, int block_size,
+                                             int max_blocks_per_seq, int64_t num_blocks,
+                                             float scale, int32_t *dev_status, void *stream) {
+  using namespace pkv;
+  if (num_seqs < 0 || total_q < 0 || max_seqlen_q < 0 || num_q_heads <= 0 ||
+      num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || max_blocks_per_seq <= 0 ||
+      num_blocks <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if (num_q_heads % num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+  const int G = num_q_heads / num_kv_heads;
+  if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return PKV_ERR_UNSUPPORTED;
+  if (block_size != 64 && block_size != 128 && block_size != 256 && block_size != 512)
+    return PKV_ERR_UNSUPPORTED;
+  if (!(scale == scale)) return PKV_ERR_INVALID_ARG;
+  if (num_seqs == 0 || total_q == 0 || max_seqlen_q == 0) return PKV_OK;
+  if (total_q > 0x7FFFFFFFLL) return PKV_ERR_UNSUPPORTED;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !cu_seqlens_q || !cu_seqlens_k)
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PKV_ERR_INVALID_ARG;
+
+  PrefillParams prm;
+  prm.out = out;
+  prm.block_tables = block_tables;
+  prm.cu_q = cu_seqlens_q;
+  prm.cu_k = cu_seqlens_k;
+  prm.status = dev_status;
+  prm.num_blocks = num_blocks;
+  prm.total_q = total_q;
+  prm.num_seqs = num_seqs;
+  prm.num_q_heads = num_q_heads;
+  prm.num_kv_heads = num_kv_heads;
+  prm.block_size = block_size;
+  prm.max_blocks_per_seq = max_blocks_per_seq;
+  prm.q_tiles = (max_seqlen_q + BM - 1) / BM;
+  prm.qscale = scale * kLog2e;
+
+  // q as {D, Hq, T}: a box is 64 dims x 1 head x 128 query rows (swizzled).
+  const uint64_t qdims[3] = {(uint64_t)head_dim, (uint64_t)num_q_heads, (uint64_t)total_q};
+  const uint64_t qstr[2] = {(uint64_t)head_dim * 2, (uint64_t)num_q_heads * head_dim * 2};
+  const uint32_t qbox[3] = {64u, 1u, (uint32_t)BM};
+  // cache as {D, Hkv, block_size, NB}: a box is 64 dims x 1 head x 64 tokens x 1 block.
+  const uint64_t kdims[4] = {(uint64_t)head_dim, (uint64_t)num_kv_heads, (uint64_t)block_size,
+                             (uint64_t)num_blocks};
+  const uint64_t kstr[3] = {(uint64_t)head_dim * 2, (uint64_t)num_kv_heads * head_dim * 2,
+                            (uint64_t)block_size * num_kv_heads * head_dim * 2};
+  const uint32_t kbox[4] = {64u, 1u, (uint32_t)BN, 1u};
+  CUtensorMap tq, tk, tv;
+  if (!encode_bf16_map(&tq, q, 3, qdims, qstr, qbox, true) ||
+      !encode_bf16_map(&tk, k_cache, 4, kdims, kstr, kbox, true) ||
+      !encode_bf16_map(&tv, v_cache, 4, kdims, kstr, kbox, true))
+    return PKV_ERR_CUDA;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool pair = (G % 2) == 0;
+  if (head_dim == 128) return pair ? launch_prefill<128, 2>(tq, tk, tv, prm, st)
+                                   : launch_prefill<128, 1>(tq, tk, tv, prm, st);
+  return pair ? launch_prefill<64, 2>(tq, tk, tv, prm, st) : launch_prefill<64, 1>(tq, tk, tv, prm, st);
+}

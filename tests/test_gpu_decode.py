@@ -1,0 +1,114 @@
+"""Paged decode attention on the GPU against the fp64 oracle.
+
+Tolerance: |gpu - oracle| <= 8e-3 + 1e-2 |oracle| elementwise (bf16 inputs,
+fp32 accumulation, bf16 output)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from gpu_util import DeviceBatch, assert_close, bf16, bits, i32, oracle_caches
+
+pytestmark = pytest.mark.gpu
+
+
+def check_decode(lib, b, seqs=None, max_total_blocks=None):
+    db = DeviceBatch(lib, b)
+    out = db.decode(max_total_blocks)
+    assert db.status_value() == 0
+    ekc, evc = oracle_caches(b)
+    want = oracle.paged_decode_attn(b.q, ekc, evc, b.block_tables, b.context_lens, b.scale,
+                                    seqs=seqs)
+    got = out.double().cpu().numpy()
+    rows = slice(None) if seqs is None else list(seqs)
+    assert_close(got[rows], want[rows], f"decode {b.name}")
+    return db, out
+
+
+def test_decode_tiny(lib):
+    check_decode(lib, wl.tiny())
+
+
+def test_decode_batch_full_size(lib):
+    check_decode(lib, wl.decode())
+
+
+def test_longdecode_sampled_sequences(lib):
+    b = wl.longdecode()
+    L = b.context_lens
+    rng = np.random.default_rng(0)
+    seqs = sorted(set([int(np.argmax(L)), int(np.argmin(L))] +
+                      rng.choice(b.num_seqs, 30, replace=False).tolist()))
+    check_decode(lib, b, seqs=seqs)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_decode_edge_lengths(lib, D, G):
+    lens = [1, 2, 63, 64, 65, 255, 256, 257, 511, 512, 513, 1000]
+    Hkv = 2
+    b = wl.build_batch("edge", "decode", 10 + G + D, [L - 1 for L in lens], [1] * len(lens),
+                       G * Hkv, Hkv, D, num_blocks=40, max_blocks_pad=3)
+    check_decode(lib, b)
+
+
+@pytest.mark.parametrize("bs", [64, 128, 512])
+def test_decode_other_block_sizes(lib, bs):
+    lens = [1, bs - 1, bs, bs + 1, 3 * bs + 5, 700]
+    b = wl.build_batch("bs", "decode", 30 + bs, [L - 1 for L in lens], [1] * len(lens), 8, 2, 128,
+                       block_size=bs)
+    check_decode(lib, b)
+
+
+def test_decode_never_reads_stale_slots(lib):
+    lens = [3, 256, 257, 300, 700]
+    b = wl.build_batch("nan", "decode", 41, [L - 1 for L in lens], [1] * len(lens), 8, 2, 128,
+                       stale="nan")
+    db, out = check_decode(lib, b)
+    assert torch.isfinite(out.float()).all()
+
+
+def test_decode_context_of_one_returns_v_bits(lib):
+    b = wl.build_batch("one", "decode", 42, [0, 0, 0], [1, 1, 1], 8, 4, 128)
+    db = DeviceBatch(lib, b)
+    out = bits(db.decode())
+    for s in range(3):
+        for h in range(8):
+            assert np.array_equal(out[s, h], b.v[s, h // 2])
+
+
+def test_decode_workspace_reuse_gives_identical_results(lib):
+    b = wl.build_batch("reuse", "decode", 43, [700, 2000, 40], [1, 1, 1], 16, 8, 128)
+    db = DeviceBatch(lib, b)
+    mtb = b.total_blocks_used
+    ws = lib.decode_workspace(b.num_seqs, 16, 8, 128, mtb)
+    outs = []
+    for _ in range(3):
+        out = torch.empty((3, 16, 128), dtype=torch.bfloat16, device="cuda")
+        lib.paged_decode_attn(out, db.q, db.k_cache, db.v_cache, db.block_tables,
+                              db.context_lens, b.scale, ws, mtb, db.status)
+        outs.append(bits(out))
+    assert db.status_value() == 0
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])
+    # tickets are left at zero
+    n_tickets = b.num_seqs * b.num_kv_heads
+    assert int(ws[: n_tickets * 4].view(torch.int32).abs().sum().item()) == 0
+
+
+def test_decode_flags_bad_context_block_and_workspace(lib):
+    b = wl.build_batch("err", "decode", 44, [10, 300], [1, 1], 4, 2, 64, num_blocks=6)
+    db = DeviceBatch(lib, b)
+    # a zero-length context
+    db.context_lens[0] = 0
+    db.decode()
+    assert db.status_value() & lib.DEV_BAD_CONTEXT
+    # a block id outside the pool
+    db = DeviceBatch(lib, b)
+    db.block_tables[1, 1] = 1000
+    db.decode()
+    assert db.status_value() & lib.DEV_BAD_BLOCK
+    # more blocks than the workspace bound
+    db = DeviceBatch(lib, b)
+    db.decode(max_total_blocks=1)
+    assert db.status_value() & lib.DEV_WORKSPACE

@@ -1,0 +1,98 @@
+"""Paged varlen causal prefill on the GPU (tcgen05 path) against the fp64 oracle.
+
+Tolerance: |gpu - oracle| <= 8e-3 + 1e-2 |oracle| elementwise."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from gpu_util import DeviceBatch, assert_close, bits, oracle_caches
+
+pytestmark = pytest.mark.gpu
+
+
+def check_prefill(lib, b, rows=None):
+    db = DeviceBatch(lib, b)
+    out = db.prefill()
+    assert db.status_value() == 0
+    ekc, evc = oracle_caches(b)
+    want = oracle.paged_prefill_attn(b.q, ekc, evc, b.block_tables, b.cu_seqlens_q,
+                                     b.cu_seqlens_k, b.scale, rows=rows)
+    got = out.double().cpu().numpy()
+    sel = slice(None) if rows is None else rows
+    assert_close(got[sel], want[sel], f"prefill {b.name}")
+    return db, out
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("G", [1, 2, 4])
+def test_prefill_varlen_with_prefix_small(lib, D, G):
+    cached = [0, 256, 0, 512, 3, 0, 100]
+    new = [1, 64, 127, 128, 129, 300, 200]
+    b = wl.build_batch("small", "prefill", 50 + D + G, cached, new, 2 * G, 2, D,
+                       max_blocks_pad=2)
+    check_prefill(lib, b)
+
+
+def test_prefill_single_long_prompt(lib):
+    b = wl.build_batch("long", "prefill", 60, [0], [1500], 4, 2, 128)
+    check_prefill(lib, b)
+
+
+@pytest.mark.parametrize("bs", [64, 128, 512])
+def test_prefill_other_block_sizes(lib, bs):
+    b = wl.build_batch("bs", "prefill", 61 + bs, [0, bs, 2 * bs + 7], [200, 70, 129], 4, 2, 128,
+                       block_size=bs)
+    check_prefill(lib, b)
+
+
+def test_prefill_never_reads_stale_slots(lib):
+    b = wl.build_batch("nan", "prefill", 62, [0, 256, 5], [100, 37, 300], 4, 2, 128, stale="nan")
+    db, out = check_prefill(lib, b)
+    assert torch.isfinite(out.float()).all()
+
+
+def test_prefill_first_row_returns_first_value(lib):
+    b = wl.build_batch("first", "prefill", 63, [0, 0], [130, 7], 4, 2, 128)
+    db = DeviceBatch(lib, b)
+    out = bits(db.prefill())
+    for s, row in enumerate(b.cu_seqlens_q[:-1]):
+        for h in range(4):
+            assert np.array_equal(out[row, h], b.v[row, h // 2])
+
+
+def test_prefill_last_row_matches_decode(lib):
+    b = wl.build_batch("pd", "prefill", 64, [0, 256, 40], [300, 90, 1], 8, 2, 128)
+    db = DeviceBatch(lib, b)
+    pre = db.prefill().double().cpu().numpy()
+    last = b.cu_seqlens_q[1:] - 1
+    q_last = db.q[torch.as_tensor(last, dtype=torch.long, device="cuda")].contiguous()
+    ws = lib.decode_workspace(b.num_seqs, 8, 2, 128, b.total_blocks_used)
+    dec = torch.empty_like(q_last)
+    lib.paged_decode_attn(dec, q_last, db.k_cache, db.v_cache, db.block_tables, db.context_lens,
+                          b.scale, ws, b.total_blocks_used, db.status)
+    assert db.status_value() == 0
+    # both are within tolerance of the same oracle value: within twice of each other
+    d = dec.double().cpu().numpy()
+    assert np.all(np.abs(pre[last] - d) <= 2 * (8e-3 + 1e-2 * np.abs(d)))
+
+
+def test_prefill_full_size_sampled_rows(lib):
+    b = wl.prefill()
+    rows = wl.sample_rows(np.random.default_rng(1), b, per_seq=6)
+    check_prefill(lib, b, rows=rows)
+
+
+def test_prefix_cached_full_size_sampled_rows(lib):
+    b = wl.prefix()
+    rows = wl.sample_rows(np.random.default_rng(2), b, per_seq=6)
+    check_prefill(lib, b, rows=rows)
+
+
+def test_prefill_flags_inconsistent_seqlens(lib):
+    b = wl.build_batch("bad", "prefill", 65, [0, 0], [50, 60], 4, 2, 128)
+    db = DeviceBatch(lib, b)
+    db.cu_k[2] = db.cu_k[1] + 10  # second sequence: fewer keys than queries
+    db.prefill()
+    assert db.status_value() & lib.DEV_BAD_SEQLEN
