@@ -20,9 +20,10 @@
  * --------------------------------
  *  - bf16 tensors are passed as pointers to their 16-bit patterns.
  *  - Every pointer argument except `dev_status` and `stream` is a DEVICE
- *    pointer owned by the caller; the library allocates no memory, keeps no
- *    reference after the call returns, and only caches small per-device
- *    tables (the SM count).
+ *    pointer owned by the caller; no call allocates memory or keeps a
+ *    reference after it returns.  The library caches small per-device tables
+ *    (the SM count) and, loaded on a GPU, holds one fixed 16 MiB device array
+ *    (the scratch of pkv_paged_decode_attn_noalloc).
  *  - Layouts (all row-major, contiguous):
  *      q             [T_q, Hq, D]
  *      k, v          [T_new, Hkv, D]   (token stride configurable in kv_store)
@@ -133,6 +134,42 @@ pkv_status pkv_paged_decode_attn(uint16_t *out, const uint16_t *q, const uint16_
                                  int max_blocks_per_seq, int64_t num_blocks,
                                  int64_t max_total_blocks, float scale, void *workspace,
                                  size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/*
+ * paged_decode_attn_noalloc -- paged_decode_attn without a caller workspace.
+ *
+ * The pages have no counterpart to this call; it exists for callers of this
+ * library that cannot allocate device memory for a workspace: code running
+ * under a host framework whose allocator owns all device memory and offers no
+ * hook, a plugin that may not allocate inside its host process, or a serving
+ * loop that must keep cudaMalloc/cudaFree (which synchronise the device) off
+ * its latency path.
+ *
+ * The split-K scratch lives in a fixed 16 MiB array in the library's own
+ * device memory, which every GPU that loads the library holds until the
+ * process exits.  A call whose workspace need,
+ * pkv_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+ * max_total_blocks), exceeds 16 MiB returns PKV_ERR_WORKSPACE and launches
+ * nothing.  The call itself allocates nothing.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  Each call clears the scratch's counters with a
+ * cudaMemsetAsync on `stream`, then runs the same kernel as
+ * pkv_paged_decode_attn.  All calls on a device share the one array, so calls
+ * that overlap on the GPU (other streams, other host threads) race and
+ * corrupt each other's results: serialise them.
+ *
+ * Arguments, layouts, results and errors are those of pkv_paged_decode_attn.
+ */
+pkv_status pkv_paged_decode_attn_noalloc(uint16_t *out, const uint16_t *q,
+                                         const uint16_t *k_cache, const uint16_t *v_cache,
+                                         const int32_t *block_tables,
+                                         const int32_t *context_lens, int num_seqs,
+                                         int num_q_heads, int num_kv_heads, int head_dim,
+                                         int block_size, int max_blocks_per_seq,
+                                         int64_t num_blocks, int64_t max_total_blocks,
+                                         float scale, int32_t *dev_status, void *stream);
 
 /*
  * paged_prefill_attn -- causal attention of packed variable-length prompts

@@ -42,6 +42,9 @@ SIGNATURES = {
     "pkv_decode_workspace_size": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_i64]),
     "pkv_paged_decode_attn": (_c_int, [_p, _p, _p, _p, _p, _p, _c_int, _c_int, _c_int, _c_int,
                                        _c_int, _c_int, _c_i64, _c_i64, _c_f, _p, _c_sz, _p, _p]),
+    "pkv_paged_decode_attn_noalloc": (_c_int, [_p, _p, _p, _p, _p, _p, _c_int, _c_int, _c_int,
+                                               _c_int, _c_int, _c_int, _c_i64, _c_i64, _c_f, _p,
+                                               _p]),
     "pkv_paged_prefill_attn": (_c_int, [_p, _p, _p, _p, _p, _p, _p, _c_int, _c_i64, _c_int,
                                         _c_int, _c_int, _c_int, _c_int, _c_int, _c_i64, _c_f, _p,
                                         _p]),
@@ -163,6 +166,29 @@ def paged_decode_attn(out, q, k_cache, v_cache, block_tables, context_lens, scal
         float(scale), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _ptr(dev_status), _stream(stream))
     _check(st, "pkv_paged_decode_attn")
+
+
+def paged_decode_attn_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                              max_total_blocks, dev_status=None, stream=None) -> None:
+    """paged_decode_attn for callers that cannot allocate a workspace: the
+    scratch is a fixed 16 MiB array inside the library (see include/pkv.h).
+    Calls that overlap on the GPU must not be issued: they share that array."""
+    import torch
+
+    lib = load()
+    for name, t, dt, nd in (("out", out, torch.bfloat16, 3), ("q", q, torch.bfloat16, 3),
+                            ("k_cache", k_cache, torch.bfloat16, 4),
+                            ("v_cache", v_cache, torch.bfloat16, 4),
+                            ("block_tables", block_tables, torch.int32, 2),
+                            ("context_lens", context_lens, torch.int32, 1)):
+        _need(t, dt, name, nd)
+    S, Hq, D = q.shape
+    NB, BS, Hkv, _ = k_cache.shape
+    st = lib.pkv_paged_decode_attn_noalloc(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+        _ptr(context_lens), S, Hq, Hkv, D, BS, block_tables.shape[1], NB, int(max_total_blocks),
+        float(scale), _ptr(dev_status), _stream(stream))
+    _check(st, "pkv_paged_decode_attn_noalloc")
 
 
 def paged_prefill_attn(out, q, k_cache, v_cache, block_tables, cu_seqlens_q, cu_seqlens_k,

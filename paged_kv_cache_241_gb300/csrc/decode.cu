@@ -27,6 +27,8 @@
 //    that fits one block skips the workspace.
 #include <math.h>
 
+#include <mutex>
+
 #include "host_common.h"
 #include "pkv_common.cuh"
 
@@ -693,4 +695,81 @@ extern "C" pkv_status pkv_paged_decode_attn(uint16_t *out, const uint16_t *q,
   PKV_DECODE_CASE(128, 8)
 #undef PKV_DECODE_CASE
   return PKV_ERR_UNSUPPORTED;
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant.
+//
+// Some callers cannot hand this library a device workspace: a host framework
+// whose allocator owns all device memory and offers no hook, a plugin that is
+// not allowed to allocate inside the host process, or a serving loop that
+// must not call cudaMalloc/cudaFree on its latency path because those calls
+// synchronise the device.  For them, the decode scratch (tickets and split-K
+// partials) lives in one fixed array in the library's own device memory.
+// ---------------------------------------------------------------------------
+
+namespace pkv {
+namespace {
+constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;  // 16 MiB per device
+}  // namespace
+}  // namespace pkv
+
+// Loaded with the library on every GPU it runs on and held until exit.
+static __device__ __align__(256) uint8_t pkv_decode_scratch[pkv::kNoAllocScratchBytes];
+
+namespace pkv {
+namespace {
+
+std::mutex g_scratch_mu;
+void *g_scratch_ptr[64] = {nullptr};
+
+// Device address of pkv_decode_scratch on the current device.  In host code
+// the array's name is only a host-side stand-in, so the address is looked up
+// once per device (with that device current) and cached.
+pkv_status scratch_for_current_device(void **ptr) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return PKV_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, pkv_decode_scratch) != cudaSuccess || p == nullptr)
+      return PKV_ERR_CUDA;
+    g_scratch_ptr[dev] = p;
+  }
+  *ptr = g_scratch_ptr[dev];
+  return PKV_OK;
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" pkv_status pkv_paged_decode_attn_noalloc(
+    uint16_t *out, const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+    const int32_t *block_tables, const int32_t *context_lens, int num_seqs, int num_q_heads,
+    int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq, int64_t num_blocks,
+    int64_t max_total_blocks, float scale, int32_t *dev_status, void *stream) {
+  using namespace pkv;
+  if (max_total_blocks > (int64_t)kNoAllocScratchBytes) return PKV_ERR_WORKSPACE;
+  const size_t need =
+      pkv_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_total_blocks);
+  if (need == 0) {
+    // Bad sizes or an empty batch: the regular entry point reports it.
+    return pkv_paged_decode_attn(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                                 num_q_heads, num_kv_heads, head_dim, block_size,
+                                 max_blocks_per_seq, num_blocks, max_total_blocks, scale,
+                                 nullptr, 0, dev_status, stream);
+  }
+  if (need > kNoAllocScratchBytes) return PKV_ERR_WORKSPACE;
+  void *scratch = nullptr;
+  const pkv_status st = scratch_for_current_device(&scratch);
+  if (st != PKV_OK) return st;
+  // The array keeps the previous call's contents: clear the ticket counters.
+  const size_t tickets = align256((size_t)num_seqs * num_kv_heads * 4);
+  if (cudaMemsetAsync(scratch, 0, tickets, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  return pkv_paged_decode_attn(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                               num_q_heads, num_kv_heads, head_dim, block_size,
+                               max_blocks_per_seq, num_blocks, max_total_blocks, scale, scratch,
+                               kNoAllocScratchBytes, dev_status, stream);
 }
