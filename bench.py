@@ -345,6 +345,30 @@ def run_reference(args):
     print(json.dumps(line))
     return 0
 
+DEFAULT_COPIES = {"decode": 4, "longdecode": 3, "prefill": 4, "prefix": 8}
+MAKERS = {"decode": wl.decode, "longdecode": wl.longdecode, "prefill": wl.prefill,
+          "prefix": wl.prefix}
+
+
+def run_single(args, pkv, dev, peaks, peak_src):
+    """One workload alone: `steps` timed steps of store + attention."""
+    b = MAKERS[args.workload](fill_cache=False)
+    arm = Arm(pkv, b, dev, copies=args.copies or DEFAULT_COPIES[args.workload])
+    total, am, sm_ = arm.run(args.steps, args.warmup)
+    rec = {"workload": args.workload, "steps": args.steps, "warmup": args.warmup,
+           "copies": len(arm.copies), "ms_per_step": total / args.steps, "attn_kernel_ms": am,
+           "kv_store_ms": sm_, "peak_source": peak_src}
+    if b.kind == "decode":
+        ach = decode_bytes(b) / (am * 1e-3) / 1e9
+        rec.update(metric="decode GB/s", value=ach, unit="GB/s",
+                   frac=ach / peaks["hbm_gbs"], bytes=decode_bytes(b))
+    else:
+        tf = prefill_flops(b) / (am * 1e-3) / 1e12
+        rec.update(metric="prefill TFLOP/s", value=tf, unit="TFLOP/s",
+                   frac=tf / peaks["bf16_tflops"], flops=prefill_flops(b))
+    print(json.dumps(rec))
+    return 0
+
 
 def main():
     ap = argparse.ArgumentParser()
@@ -353,7 +377,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only-main", action="store_true")
+    ap.add_argument("--only-main", action="store_true",
+                    help="headline decode step only (no other workloads)")
+    ap.add_argument("--workload", default="all",
+                    choices=["all", "decode", "longdecode", "prefill", "prefix"],
+                    help="run one workload alone (small runs for profiling)")
+    ap.add_argument("--copies", type=int, default=0,
+                    help="rotating cache copies (0 = the default for each workload)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -389,9 +419,12 @@ def main():
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         return float(t.item())
 
+    if args.workload != "all":
+        return run_single(args, pkv, dev, peaks, peak_src)
+
     # ---- headline: decode batch (4 rotating copies of the 1 GiB pool) ----
     b = wl.decode(fill_cache=False)
-    arm = Arm(pkv, b, dev, copies=4)
+    arm = Arm(pkv, b, dev, copies=args.copies or 4)
     sampler.start()
     barrier()
     total_ms, attn_ms, store_ms = arm.run(args.steps, args.warmup)
@@ -404,9 +437,10 @@ def main():
     extra = {}
     if not args.only_main:
         # ---- other workloads of the path ----
-        for name, make, copies, steps in (("longdecode", wl.longdecode, 3, 200),
-                                          ("prefill", wl.prefill, 4, 100),
-                                          ("prefix", wl.prefix, 8, 300)):
+        sub = max(20, args.steps // 10)
+        for name, make, copies, steps in (("longdecode", wl.longdecode, 3, sub),
+                                          ("prefill", wl.prefill, 4, sub),
+                                          ("prefix", wl.prefix, 8, sub)):
             bb = make(fill_cache=False)
             a2 = Arm(pkv, bb, dev, copies=copies)
             tot, am, sm_ = a2.run(steps, args.warmup)
