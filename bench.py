@@ -481,11 +481,11 @@ def main():
                    "step_bytes": step_bytes},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
-                     "kernel": "paged_decode_kernel<128,2>", "peak_source": peak_src,
+                     "kernel": "paged_decode_kernel<128,2> + decode_merge_kernel<128,2>", "peak_source": peak_src,
                      "attn_kernel_ms": attn_ms, "kv_store_ms": store_ms},
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": 3 * args.steps,  # kv_store, split-K decode, merge
         "clocks": clocks,
     }
     line.update(extra)

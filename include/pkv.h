@@ -115,14 +115,15 @@ size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads
  * g = Hq / Hkv.  bf16 in, fp32 accumulation, bf16 out (round to nearest even).
  *
  * Split-K flash-decoding: each (sequence, kv head, block) is one work item
- * whose partial (max, sum, unnormalised output) goes to the workspace; the
- * last item of a (sequence, kv head) to finish merges them.
+ * whose partial (max, sum, unnormalised output) goes to the workspace; a
+ * second kernel, launched as a programmatic dependent of the first, merges
+ * the partials of every sequence that spans more than one block.  Two kernel
+ * launches per call (one when max_blocks_per_seq == 1).
  *
  * workspace: device buffer of at least pkv_decode_workspace_size(...) bytes,
- * 256-byte aligned, ZERO-FILLED before its first use.  Every call leaves its
- * counters at zero again, so it can be reused without clearing; after a call
- * that reported PKV_DEV_TIMEOUT, zero it again.  Calls that overlap on the
- * device must not share a workspace.
+ * 256-byte aligned.  Its contents need no initialisation: every call writes
+ * each entry before reading it.  Calls that overlap on the device must not
+ * share a workspace.
  *
  * Supported: head_dim in {64, 128}; Hq/Hkv in {1, 2, 4, 8}; block_size in
  * {64, 128, 256, 512}; num_seqs <= 16384.
@@ -154,10 +155,11 @@ pkv_status pkv_paged_decode_attn(uint16_t *out, const uint16_t *q, const uint16_
  *
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.  Each call clears the scratch's counters with a
- * cudaMemsetAsync on `stream`, then runs the same kernel as
- * pkv_paged_decode_attn.  All calls on a device share the one array, so calls
- * that overlap on the GPU (other streams, other host threads) race and
+ * before any stream capture.  Each call then runs the same kernels as
+ * pkv_paged_decode_attn on that array; the array keeps the previous call's
+ * contents, but nothing in it needs to start at zero (each call writes every
+ * entry before reading it).  All calls on a device share the one array, so
+ * calls that overlap on the GPU (other streams, other host threads) race and
  * corrupt each other's results: serialise them.
  *
  * Arguments, layouts, results and errors are those of pkv_paged_decode_attn.

@@ -38,7 +38,7 @@ namespace {
 constexpr int kTile = 64;           // tokens per TMA tile
 constexpr int kConsumerWarps = 4;   // compute warps per CTA
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStages = 3;          // shared-memory tile ring
+constexpr int kStages = 4;          // shared-memory tile ring
 constexpr int kMaxSeqs = 16384;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -47,7 +47,7 @@ struct DecodeParams {
   const uint16_t *q;
   const int32_t *block_tables;
   const int32_t *context_lens;
-  int32_t *tickets;   // [num_seqs * Hkv]
+  int32_t *seq_prefix;  // [num_seqs + 1]: first partial (block) index of each sequence
   float *part_ml;     // [max_total_blocks, Hq, 2]   (max in log2 units, sum)
   float *part_o;      // [max_total_blocks, Hq, D]
   int32_t *status;
@@ -172,24 +172,37 @@ __device__ __forceinline__ void load_probs(const float *p, float (&pv)[G]) {
 
 // Shared-memory carve-up (bytes), shared by host and device.
 struct DecodeSmem {
-  int tiles, bars, logits, red, stats, misc, prefix, total;
+  int tiles, qbuf, bars, logits, red, stats, misc, prefix, ctx, total;
   __host__ __device__ DecodeSmem(int D, int G, int bs, int num_seqs) {
     tiles = 0;
-    bars = tiles + kStages * kTile * D * 2;
-    logits = bars + 2 * kStages * 8;
+    qbuf = tiles + kStages * kTile * D * 2;  // [2][G*D] bf16: q of the next items
+    bars = qbuf + 2 * G * D * 2;             // full[S], empty[S], q_full[2], q_empty[2]
+    logits = bars + (2 * kStages + 4) * 8;
     red = logits + ((bs * G * 4 + 15) & ~15);
     stats = red + kConsumerWarps * G * D * 4;
     misc = stats + 2 * G * 4;
     prefix = misc + 16;
-    total = prefix + (num_seqs + 1) * 4;
+    ctx = prefix + (num_seqs + 1) * 4;
+    total = ctx + num_seqs * 4;
   }
 };
+
+// 1-D bulk copy global -> shared, completing on an mbarrier (16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes,
+                                          uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
 
 template <int D, int G>
 __global__ void __launch_bounds__(kThreads)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
   constexpr int kTileBytes = kTile * D * 2;
+  constexpr int kQBytes = G * D * 2;
   constexpr int CPL = D / 64;  // 16-byte chunks per lane per token (phase 1)
   constexpr int DPL = D / 32;  // output dims per lane (phase 3)
   constexpr int NV = 4 * G;    // partial dot products per lane (phase 1)
@@ -199,14 +212,18 @@ __global__ void __launch_bounds__(kThreads)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const DecodeSmem lay(D, G, p.block_size, p.num_seqs);
   uint8_t *tiles = smem + lay.tiles;
+  uint8_t *qbuf = smem + lay.qbuf;
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + lay.bars);
   uint64_t *empty = full + kStages;
+  uint64_t *q_full = empty + kStages;
+  uint64_t *q_empty = q_full + 2;
   float *logits = reinterpret_cast<float *>(smem + lay.logits);  // [block_size][G]
   float *red = reinterpret_cast<float *>(smem + lay.red);        // [warps][G][D]
   float *mstat = reinterpret_cast<float *>(smem + lay.stats);    // [G]
   float *lstat = mstat + G;                                      // [G]
-  int *misc = reinterpret_cast<int *>(smem + lay.misc);          // abort, last, total
+  int *misc = reinterpret_cast<int *>(smem + lay.misc);          // abort flag
   int *prefix = reinterpret_cast<int *>(smem + lay.prefix);      // [num_seqs + 1]
+  int *ctx = reinterpret_cast<int *>(smem + lay.ctx);            // [num_seqs], clamped
   volatile int *abort_flag = misc;
 
   const int tid = threadIdx.x;
@@ -216,15 +233,19 @@ __global__ void __launch_bounds__(kThreads)
   const int BS = p.block_size;
   const int Hkv = p.num_kv_heads;
   const int Hq = p.num_q_heads;
+  const int max_ctx = p.max_blocks_per_seq * BS;
 
-  // ---- prologue: barriers, and the block prefix over sequences -----------
+  // ---- prologue: barriers, clamped lengths and the block prefix -----------
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kConsumerWarps);
     }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], kConsumerWarps);
+    }
     misc[0] = 0;
-    misc[1] = 0;
     fence_barrier_init();
   }
   if (tid == kConsumerWarps * 32) {
@@ -236,8 +257,11 @@ __global__ void __launch_bounds__(kThreads)
   const int s_end = min(s_begin + per, S);
   int bad = 0;
   int local = 0;
-  for (int s = s_begin; s < s_end; ++s)
-    local += seq_blocks(p.context_lens[s], BS, p.max_blocks_per_seq, &bad);
+  for (int s = s_begin; s < s_end; ++s) {
+    const int L = p.context_lens[s];
+    ctx[s] = L <= 0 ? 0 : min(L, max_ctx);
+    local += seq_blocks(L, BS, p.max_blocks_per_seq, &bad);
+  }
   if (bad && blockIdx.x == 0) flag_status(p.status, PKV_DEV_BAD_CONTEXT);
   int incl = local;
 #pragma unroll
@@ -257,19 +281,25 @@ __global__ void __launch_bounds__(kThreads)
   }
   {
     int run = offset;
-    int dummy = 0;
     for (int s = s_begin; s < s_end; ++s) {
       prefix[s] = run;
-      run += seq_blocks(p.context_lens[s], BS, p.max_blocks_per_seq, &dummy);
+      run += (ctx[s] + BS - 1) / BS;
     }
     if (tid == 0) prefix[S] = total;
   }
   __syncthreads();
-  if ((int64_t)total > p.max_total_blocks) {
+  // Block 0 publishes the prefix for the merge kernel (all zeros, i.e. nothing
+  // to merge, when the workspace bound is exceeded).
+  const bool overflow = (int64_t)total > p.max_total_blocks;
+  if (blockIdx.x == 0)
+    for (int i = tid; i <= S; i += kThreads) p.seq_prefix[i] = overflow ? 0 : prefix[i];
+  if (overflow) {
     if (blockIdx.x == 0 && tid == 0) flag_status(p.status, PKV_DEV_WORKSPACE);
     return;
   }
   const int total_items = total * Hkv;
+  // The merge kernel may start launching now; it waits for this grid to finish.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   auto item_coords = [&](int w, int &s, int &b, int &j, int &gblk) {
     gblk = w / Hkv;
@@ -286,23 +316,43 @@ __global__ void __launch_bounds__(kThreads)
     b = gblk - prefix[s];
   };
 
-  // ---- producer warp: TMA K tiles then V tiles of every item ---------------
+  // ---- producer warp: q, then K tiles, then V tiles of every item ----------
   if (warp == kConsumerWarps) {
     if (lane == 0) {
       const uint64_t policy = l2_policy_evict_first();
       int issued = 0;
+      int item_no = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < total_items && ok; w += gridDim.x) {
-        int s, b, j, gblk;
+      int s, b, j, gblk;
+      int blk_next = 0;
+      if (blockIdx.x < total_items) {
+        item_coords(blockIdx.x, s, b, j, gblk);
+        blk_next = p.block_tables[(int64_t)s * p.max_blocks_per_seq + b];
+      }
+      for (int w = blockIdx.x; w < total_items && ok; w += gridDim.x, ++item_no) {
         item_coords(w, s, b, j, gblk);
-        const int L = min(p.context_lens[s], p.max_blocks_per_seq * BS);
-        const int valid = min(BS, L - b * BS);
-        const int ntile = (valid + kTile - 1) / kTile;
-        int blk = p.block_tables[(int64_t)s * p.max_blocks_per_seq + b];
+        int blk = blk_next;
+        const int wn = w + gridDim.x;
+        if (wn < total_items) {  // fetch the next item's block id early
+          int sn, bn, jn, gn;
+          item_coords(wn, sn, bn, jn, gn);
+          blk_next = p.block_tables[(int64_t)sn * p.max_blocks_per_seq + bn];
+        }
         if (blk < 0 || (int64_t)blk >= p.num_blocks) {
           flag_status(p.status, PKV_DEV_BAD_BLOCK);
           blk = 0;
         }
+        const int valid = min(BS, ctx[s] - b * BS);
+        const int ntile = (valid + kTile - 1) / kTile;
+        const int qb = item_no & 1;
+        if (item_no >= 2 &&
+            !mbar_wait_bounded(&q_empty[qb], ((item_no >> 1) - 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&q_full[qb], kQBytes);
+        bulk_load(qbuf + qb * kQBytes, p.q + ((int64_t)s * Hq + j * G) * D, kQBytes,
+                  &q_full[qb]);
         for (int half = 0; half < 2 && ok; ++half) {
           const CUtensorMap *map = half ? &tm_v : &tm_k;
           for (int t = 0; t < ntile; ++t) {
@@ -323,6 +373,8 @@ __global__ void __launch_bounds__(kThreads)
       // Do not leave while copies into this CTA's shared memory are in flight.
       for (int i = max(0, issued - kStages); i < issued; ++i)
         mbar_wait_bounded(&full[i % kStages], (i / kStages) & 1, nullptr);
+      for (int i = max(0, item_no - 2); i < item_no; ++i)
+        mbar_wait_bounded(&q_full[i & 1], (i >> 1) & 1, nullptr);
     }
     return;
   }
@@ -331,24 +383,27 @@ __global__ void __launch_bounds__(kThreads)
   const int r = lane & 7;     // lane within its octet
   const int gid = lane >> 3;  // octet index: 4 tokens each
   int ctile = 0;              // tiles consumed so far
-  for (int w = blockIdx.x; w < total_items; w += gridDim.x) {
+  int item_no = 0;
+  for (int w = blockIdx.x; w < total_items; w += gridDim.x, ++item_no) {
     int s, b, j, gblk;
     item_coords(w, s, b, j, gblk);
-    const int L = min(p.context_lens[s], p.max_blocks_per_seq * BS);
-    const int valid = min(BS, L - b * BS);
+    const int valid = min(BS, ctx[s] - b * BS);
     const int ntile = (valid + kTile - 1) / kTile;
     const int nblk = prefix[s + 1] - prefix[s];
     const int h0 = j * G;
 
-    // q fragment: dims of chunks r + 8c, pre-scaled into log2 units.
+    // q fragment from the staged copy: dims of chunks r + 8c, in log2 units.
     float qf[G][CPL * 8];
     {
-      const uint16_t *qrow = p.q + ((int64_t)s * Hq + h0) * D;
+      const int qb = item_no & 1;
+      const bool ok = mbar_wait_bounded(&q_full[qb], (item_no >> 1) & 1, abort_flag);
+      const uint16_t *qs = reinterpret_cast<const uint16_t *>(qbuf + qb * kQBytes);
 #pragma unroll
       for (int h = 0; h < G; ++h) {
 #pragma unroll
         for (int c = 0; c < CPL; ++c) {
-          const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(qrow + h * D + (r + 8 * c) * 8));
+          uint4 raw = make_uint4(0, 0, 0, 0);
+          if (ok) raw = *reinterpret_cast<const uint4 *>(qs + h * D + (r + 8 * c) * 8);
           const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -357,6 +412,8 @@ __global__ void __launch_bounds__(kThreads)
           }
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&q_empty[qb]);
     }
 
     // Phase 1: logits of the item's tokens.
@@ -503,59 +560,6 @@ __global__ void __launch_bounds__(kThreads)
         p.part_ml[((int64_t)gblk * Hq + h0 + tid) * 2] = mstat[tid];
         p.part_ml[((int64_t)gblk * Hq + h0 + tid) * 2 + 1] = lstat[tid];
       }
-      __threadfence();
-      named_bar_sync(1, kConsumerWarps * 32);
-      if (tid == 0) {
-        const unsigned old =
-            atomicInc(reinterpret_cast<unsigned *>(p.tickets + (int64_t)s * Hkv + j),
-                      (unsigned)(nblk - 1));
-        misc[1] = (old == (unsigned)(nblk - 1)) ? 1 : 0;
-      }
-      named_bar_sync(1, kConsumerWarps * 32);
-      if (misc[1]) {
-        // Last partial of (s, j): merge all nblk partials.
-        __threadfence();
-        const int pb0 = prefix[s];
-        for (int h = warp; h < G; h += kConsumerWarps) {
-          float M = -INFINITY;
-          for (int bb = lane; bb < nblk; bb += 32)
-            M = fmaxf(M, __ldcg(p.part_ml + ((int64_t)(pb0 + bb) * Hq + h0 + h) * 2));
-          M = warp_max(M);
-          float Ls = 0.f;
-          for (int bb = lane; bb < nblk; bb += 32) {
-            const float *ml = p.part_ml + ((int64_t)(pb0 + bb) * Hq + h0 + h) * 2;
-            Ls += fast_exp2(__ldcg(ml) - M) * __ldcg(ml + 1);
-          }
-          Ls = warp_sum(Ls);
-          if (lane == 0) {
-            mstat[h] = M;
-            lstat[h] = 1.f / Ls;
-          }
-        }
-        named_bar_sync(1, kConsumerWarps * 32);
-        for (int idx = tid; idx < G * D / 4; idx += kConsumerWarps * 32) {
-          const int e = idx * 4;
-          const int h = e / D;
-          const float M = mstat[h];
-          float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-          for (int bb = 0; bb < nblk; ++bb) {
-            const int64_t row = (int64_t)(pb0 + bb) * Hq + h0 + h;
-            const float wgt = fast_exp2(__ldcg(p.part_ml + row * 2) - M);
-            const float4 x = __ldcg(reinterpret_cast<const float4 *>(p.part_o + row * D + e - h * D));
-            o.x = fmaf(wgt, x.x, o.x);
-            o.y = fmaf(wgt, x.y, o.y);
-            o.z = fmaf(wgt, x.z, o.z);
-            o.w = fmaf(wgt, x.w, o.w);
-          }
-          const float inv = lstat[h];
-          uint16_t *dst = p.out + ((int64_t)s * Hq + h0) * D + e;
-          uint2 packed;
-          packed.x = pack_bf16x2(o.x * inv, o.y * inv);
-          packed.y = pack_bf16x2(o.z * inv, o.w * inv);
-          *reinterpret_cast<uint2 *>(dst) = packed;
-        }
-      }
     }
     // All consumer warps agree on whether to stop (a wait ran out).
     if (named_bar_or(1, kConsumerWarps * 32, *abort_flag != 0)) {
@@ -563,6 +567,90 @@ __global__ void __launch_bounds__(kThreads)
       break;
     }
   }
+}
+
+// Split-K merge: one CTA per (sequence, kv head) with more than one block.
+// M = max_b m_b;  O = sum_b 2^(m_b - M) o_b / sum_b 2^(m_b - M) l_b  (log2 units).
+// Threads are split into groups that take interleaved partials, so a long
+// context's partials are read in parallel; the groups are then summed in smem.
+constexpr int kMergeThreads = 256;
+
+template <int D, int G>
+__global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecodeParams p) {
+  // Partials are complete once the split-K grid has finished.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  constexpr int V4 = G * D / 4;  // float4 outputs per (sequence, kv head)
+  constexpr int GR = V4 >= kMergeThreads ? 1 : kMergeThreads / V4;
+  __shared__ float4 red[GR][V4];
+  __shared__ float sM[G], sInv[G];
+  const int Hkv = p.num_kv_heads;
+  const int Hq = p.num_q_heads;
+  const int s = blockIdx.x / Hkv;
+  const int j = blockIdx.x - s * Hkv;
+  const int pb0 = p.seq_prefix[s];
+  const int nblk = p.seq_prefix[s + 1] - pb0;
+  if (nblk <= 1) return;  // single-block sequences were finished by the split-K grid
+  if (pb0 < 0 || (int64_t)pb0 + nblk > p.max_total_blocks) return;  // never index past the workspace
+  const int h0 = j * G;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  for (int h = warp; h < G; h += kMergeThreads / 32) {
+    float M = -INFINITY;
+    for (int b = lane; b < nblk; b += 32)
+      M = fmaxf(M, __ldcg(p.part_ml + ((int64_t)(pb0 + b) * Hq + h0 + h) * 2));
+    M = warp_max(M);
+    float Ls = 0.f;
+    for (int b = lane; b < nblk; b += 32) {
+      const float *ml = p.part_ml + ((int64_t)(pb0 + b) * Hq + h0 + h) * 2;
+      Ls += fast_exp2(__ldcg(ml) - M) * __ldcg(ml + 1);
+    }
+    Ls = warp_sum(Ls);
+    if (lane == 0) {
+      sM[h] = M;
+      sInv[h] = 1.f / Ls;
+    }
+  }
+  __syncthreads();
+  const int v = tid % V4;
+  const int g = tid / V4;
+  const int e = v * 4;
+  const int h = e / D;
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (g < GR) {
+    const float M = sM[h];
+#pragma unroll 4
+    for (int b = g; b < nblk; b += GR) {
+      const int64_t row = (int64_t)(pb0 + b) * Hq + h0 + h;
+      const float w = fast_exp2(__ldcg(p.part_ml + row * 2) - M);
+      const float4 x = __ldcg(reinterpret_cast<const float4 *>(p.part_o + row * D + (e - h * D)));
+      o.x = fmaf(w, x.x, o.x);
+      o.y = fmaf(w, x.y, o.y);
+      o.z = fmaf(w, x.z, o.z);
+      o.w = fmaf(w, x.w, o.w);
+    }
+    if (GR > 1) red[g][v] = o;
+  }
+  if (GR > 1) {
+    __syncthreads();
+    if (tid >= V4) return;
+    o = red[0][v];
+#pragma unroll
+    for (int q = 1; q < GR; ++q) {
+      const float4 x = red[q][v];
+      o.x += x.x;
+      o.y += x.y;
+      o.z += x.z;
+      o.w += x.w;
+    }
+  } else if (tid >= V4) {
+    return;
+  }
+  const float inv = sInv[h];
+  uint2 packed;
+  packed.x = pack_bf16x2(o.x * inv, o.y * inv);
+  packed.y = pack_bf16x2(o.z * inv, o.w * inv);
+  *reinterpret_cast<uint2 *>(p.out + ((int64_t)s * Hq + h0) * D + e) = packed;
 }
 
 template <int D, int G>
@@ -594,6 +682,24 @@ pkv_status launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const Dec
   if (grid > max_items) grid = max_items;
   if (grid < 1) grid = 1;
   paged_decode_kernel<D, G><<<(unsigned)grid, kThreads, smem, stream>>>(tk, tv, prm);
+  if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+  if (prm.max_blocks_per_seq <= 1) return PKV_OK;  // nothing can need a merge
+  // The merge grid is launched as a programmatic dependent of the split-K
+  // grid: it may be scheduled early and waits (griddepcontrol.wait) for the
+  // split-K grid's completion before reading the partials.
+  const int64_t merge_grid = (int64_t)prm.num_seqs * prm.num_kv_heads;
+  if (merge_grid > 0x7FFFFFFFLL) return PKV_ERR_INVALID_ARG;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)merge_grid);
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, decode_merge_kernel<D, G>, prm) != cudaSuccess) return PKV_ERR_CUDA;
   return launch_status();
 }
 
@@ -608,7 +714,7 @@ extern "C" size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int n
   if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
       max_total_blocks < 0)
     return 0;
-  return align256((size_t)num_seqs * num_kv_heads * 4) +
+  return align256((size_t)(num_seqs + 1) * 4) +
          align256((size_t)max_total_blocks * num_q_heads * 2 * 4) +
          align256((size_t)max_total_blocks * num_q_heads * head_dim * 4);
 }
@@ -651,8 +757,8 @@ extern "C" pkv_status pkv_paged_decode_attn(uint16_t *out, const uint16_t *q,
   prm.block_tables = block_tables;
   prm.context_lens = context_lens;
   uint8_t *ws = static_cast<uint8_t *>(workspace);
-  prm.tickets = reinterpret_cast<int32_t *>(ws);
-  ws += align256((size_t)num_seqs * num_kv_heads * 4);
+  prm.seq_prefix = reinterpret_cast<int32_t *>(ws);
+  ws += align256((size_t)(num_seqs + 1) * 4);
   prm.part_ml = reinterpret_cast<float *>(ws);
   ws += align256((size_t)max_total_blocks * num_q_heads * 2 * 4);
   prm.part_o = reinterpret_cast<float *>(ws);
@@ -704,7 +810,7 @@ extern "C" pkv_status pkv_paged_decode_attn(uint16_t *out, const uint16_t *q,
 // whose allocator owns all device memory and offers no hook, a plugin that is
 // not allowed to allocate inside the host process, or a serving loop that
 // must not call cudaMalloc/cudaFree on its latency path because those calls
-// synchronise the device.  For them, the decode scratch (tickets and split-K
+// synchronise the device.  For them, the decode scratch (sequence prefix and split-K
 // partials) lives in one fixed array in the library's own device memory.
 // ---------------------------------------------------------------------------
 
@@ -764,10 +870,8 @@ extern "C" pkv_status pkv_paged_decode_attn_noalloc(
   void *scratch = nullptr;
   const pkv_status st = scratch_for_current_device(&scratch);
   if (st != PKV_OK) return st;
-  // The array keeps the previous call's contents: clear the ticket counters.
-  const size_t tickets = align256((size_t)num_seqs * num_kv_heads * 4);
-  if (cudaMemsetAsync(scratch, 0, tickets, static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return PKV_ERR_CUDA;
+  // The array keeps the previous call's contents; nothing in it has to start
+  // at zero: every call writes each entry it later reads.
   return pkv_paged_decode_attn(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
                                num_q_heads, num_kv_heads, head_dim, block_size,
                                max_blocks_per_seq, num_blocks, max_total_blocks, scale, scratch,

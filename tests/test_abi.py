@@ -50,12 +50,12 @@ def test_status_strings(lib):
 
 
 def test_workspace_size_formula(lib):
-    # tickets (S*Hkv int32) + partial max/sum (B*Hq*2 f32) + partial outputs (B*Hq*D f32),
-    # each rounded up to 256 bytes
+    # sequence prefix ((S+1) int32) + partial max/sum (B*Hq*2 f32) + partial outputs
+    # (B*Hq*D f32), each rounded up to 256 bytes
     up = lambda x: (x + 255) // 256 * 256
     S, Hq, Hkv, D, B = 64, 16, 8, 128, 300
     assert lib.pkv_decode_workspace_size(S, Hq, Hkv, D, B) == \
-        up(S * Hkv * 4) + up(B * Hq * 2 * 4) + up(B * Hq * D * 4)
+        up((S + 1) * 4) + up(B * Hq * 2 * 4) + up(B * Hq * D * 4)
     assert lib.pkv_decode_workspace_size(0, Hq, Hkv, D, B) == 0
 
 
