@@ -372,9 +372,9 @@ __global__ void __launch_bounds__(kThreads)
       if (!ok) flag_status(p.status, PKV_DEV_TIMEOUT);
       // Do not leave while copies into this CTA's shared memory are in flight.
       for (int i = max(0, issued - kStages); i < issued; ++i)
-        mbar_wait_bounded(&full[i % kStages], (i / kStages) & 1, nullptr);
+        if (!mbar_wait_bounded(&full[i % kStages], (i / kStages) & 1, nullptr)) flag_status(p.status, PKV_DEV_TIMEOUT);
       for (int i = max(0, item_no - 2); i < item_no; ++i)
-        mbar_wait_bounded(&q_full[i & 1], (i >> 1) & 1, nullptr);
+        if (!mbar_wait_bounded(&q_full[i & 1], (i >> 1) & 1, nullptr)) flag_status(p.status, PKV_DEV_TIMEOUT);
     }
     return;
   }

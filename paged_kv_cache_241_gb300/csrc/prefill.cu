@@ -10,11 +10,12 @@
 //
 // Design (GB300):
 //  * One CTA per (sequence, 128-query tile, pair of query heads of one GQA
-//    group); CTAs are ordered heaviest-tile-first.  The two heads share every
-//    K/V tile.
+//    group); CTAs are ordered sequence-major (heaviest tiles of a sequence
+//    first) so that concurrent CTAs reuse a sequence's K/V from L2.  The two
+//    heads share every K/V tile.
 //  * Warp 0 issues TMA: the Q tiles once, then K and V tiles of 64 keys as
 //    128B-swizzled 4-D boxes {64 dims, 1 head, 64 tokens, 1 block}, the block
-//    id coming from the block table, into a 2-stage ring.
+//    id coming from the block table, into a 4-stage ring.
 //  * Warp 1 issues tcgen05.mma: S_h = Q_h K^T (M=128, N=64) into tensor memory,
 //    then O_h += P_h V (M=128, N=D) with V as an MN-major operand.
 //  * Warps 2-5 (one thread per query row) read S from tensor memory, apply the
@@ -32,8 +33,10 @@ namespace {
 
 constexpr int BM = 128;  // query rows per tile (MMA M)
 constexpr int BN = 64;   // keys per tile
-constexpr int kStages = 2;
-constexpr int kThreads = 192;
+constexpr int kStages = 4;  // K/V ring depth (fills shared memory for D=128, 2 heads)
+// Warp 0: TMA producer; warp 1: MMA issuer; then one 4-warp softmax group per head.
+template <int NH>
+constexpr int threads_for() { return 64 + 128 * NH; }
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct PrefillParams {
@@ -83,7 +86,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
 }
 
 template <int D, int NH>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_for<NH>(), 1)
     paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
@@ -93,12 +96,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kSCol = TmemCols<D, NH>::kS;
 
   // ---- which tile -------------------------------------------------------
+  // Sequence-major order, each sequence's heaviest q tiles first, head groups
+  // innermost: CTAs running together share a sequence's K/V in L2.
   const int HG = p.num_q_heads / NH;
   int idx = blockIdx.x;
   const int hg = idx % HG;
   idx /= HG;
-  const int s = idx % p.num_seqs;
-  const int tr = idx / p.num_seqs;  // 0 = the sequence's last (heaviest) q tile
+  const int tr = idx % p.q_tiles;  // 0 = the sequence's last (heaviest) q tile
+  const int s = idx / p.q_tiles;
   const int q_begin = p.cu_q[s];
   const int n = p.cu_q[s + 1] - q_begin;
   const int len_k = p.cu_k[s + 1] - p.cu_k[s];
@@ -153,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int h = 0; h < NH; ++h) {
       mbar_init(&s_full[h], 1);
-      mbar_init(&p_full[h], 128);
+      mbar_init(&p_full[h], 128);  // one softmax warpgroup per head
       mbar_init(&o_done[h], 1);
     }
     mbar_init(drain, 1);
@@ -205,10 +210,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         issued = jt + 1;
       }
       // Do not leave while copies into this CTA's shared memory are in flight.
-      mbar_wait_bounded(q_full, 0, nullptr);
+      if (!mbar_wait_bounded(q_full, 0, nullptr)) flag_status(p.status, PKV_DEV_TIMEOUT);
       for (int i = max(0, issued - kStages); i < issued; ++i) {
-        mbar_wait_bounded(&k_full[i % kStages], (i / kStages) & 1, nullptr);
-        mbar_wait_bounded(&v_full[i % kStages], (i / kStages) & 1, nullptr);
+        if (!mbar_wait_bounded(&k_full[i % kStages], (i / kStages) & 1, nullptr)) flag_status(p.status, PKV_DEV_TIMEOUT);
+        if (!mbar_wait_bounded(&v_full[i % kStages], (i / kStages) & 1, nullptr)) flag_status(p.status, PKV_DEV_TIMEOUT);
       }
     }
   } else if (warp == 1) {
@@ -278,105 +283,133 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // Wait for every MMA this thread issued before tensor memory is freed.
       umma_commit(drain);
-      mbar_wait_bounded(drain, 0, nullptr);
+      if (!mbar_wait_bounded(drain, 0, nullptr)) flag_status(p.status, PKV_DEV_TIMEOUT);
     }
   } else {
-    // ================= softmax / epilogue warpgroup =================
-    const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+    // ================= softmax / epilogue: one warpgroup per head =================
+    const int h = (warp - 2) >> 2;  // the head this warpgroup serves
+    const int quarter = warp & 3;   // TMEM lane quarter this warp may access
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     const int key_limit = min(c + q0 + row, len_k - 1);  // last key this row may see
-    float m_run[NH], l_run[NH];
-#pragma unroll
-    for (int h = 0; h < NH; ++h) {
-      m_run[h] = -INFINITY;
-      l_run[h] = 0.f;
-    }
+    const float qs = p.qscale;
+    // Running max in log2 units.  It is only raised (and O rescaled) when a
+    // tile's max exceeds it by more than 8, so P stays <= 2^8; l and O share
+    // the same reference, so the final O / l is unchanged.
+    float m_ref = -INFINITY;
+    float l_run = 0.f;
     bool ok = true;
     for (int jt = 0; jt < n_kv && ok; ++jt) {
       const int key0 = jt * BN;
-      for (int h = 0; h < NH && ok; ++h) {
-        ok = warp_wait(&s_full[h], jt & 1, abort_flag);
-        if (!ok) break;
-        tc_fence_after_sync();
-        float sv[BN / 32][32];
-#pragma unroll
-        for (int hh = 0; hh < BN / 32; ++hh)
-          tmem_load32(tmem + lane_base + kSCol + h * BN + hh * 32, sv[hh]);
-        float mt = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < BN; ++i) {
-          const float x = (key0 + i <= key_limit) ? sv[i / 32][i % 32] * p.qscale : -INFINITY;
-          sv[i / 32][i % 32] = x;
-          mt = fmaxf(mt, x);
-        }
-        const float m_new = fmaxf(m_run[h], mt);
-        const float alpha = fast_exp2(m_run[h] - m_new);
-        float rs = 0.f;
-#pragma unroll
-        for (int i = 0; i < BN; ++i) {
-          sv[i / 32][i % 32] = fast_exp2(sv[i / 32][i % 32] - m_new);
-          rs += sv[i / 32][i % 32];
-        }
-        if (jt > 0) {
-          // PV of the previous tile must be complete: O is rescaled, P reused.
-          ok = warp_wait(&o_done[h], (jt - 1) & 1, abort_flag);
-          if (!ok) break;
-          tc_fence_after_sync();
-          if (__any_sync(0xffffffffu, alpha < 1.f)) {
-#pragma unroll 1
-            for (int cc = 0; cc < D / 32; ++cc) {
-              float ov[32];
-              const uint32_t oa = tmem + lane_base + kOCol + h * D + cc * 32;
-              tmem_load32(oa, ov);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) ov[i] *= alpha;
-              tmem_store32(oa, ov);
-            }
-          }
-        }
-        l_run[h] = l_run[h] * alpha + rs;
-        m_run[h] = m_new;
-        if (h == 0 && jt == n_kv - 1 && key0 + BN > len_k) {
-          // Keys past the context may hold stale bits (even NaN); P is zero
-          // there, but 0 * NaN is not, so clear those V rows first.
-          ok = warp_wait(&v_full[jt % kStages], (jt / kStages) & 1, abort_flag);
-          if (!ok) break;
-          const int first = len_k - key0;
-          uint8_t *vt = sV + (jt % kStages) * L::kKVBytes;
-          const int nchunks = (BN - first) * 8 * XR;  // 16-byte chunks to clear
-          for (int i = row; i < nchunks; i += 128) {
-            const int x = i / ((BN - first) * 8);
-            const int rem = i - x * (BN - first) * 8;
-            const int rr = first + rem / 8;
-            *reinterpret_cast<uint4 *>(vt + x * BN * 128 + rr * 128 + (rem & 7) * 16) =
-                make_uint4(0, 0, 0, 0);
-          }
-        }
-        // P (bf16) into the 128B-swizzled K-major tile: row `row`, 16-byte chunk c
-        // of keys 8c..8c+7 lands at chunk c ^ (row & 7).
-        uint8_t *prow = sP + h * L::kPBytes + row * 128;
-#pragma unroll
-        for (int cidx = 0; cidx < BN / 8; ++cidx) {
-          uint4 w;
-          const float *pv = &sv[cidx / 4][(cidx % 4) * 8];
-          w.x = pack_bf16x2(pv[0], pv[1]);
-          w.y = pack_bf16x2(pv[2], pv[3]);
-          w.z = pack_bf16x2(pv[4], pv[5]);
-          w.w = pack_bf16x2(pv[6], pv[7]);
-          *reinterpret_cast<uint4 *>(prow + ((cidx ^ (row & 7)) * 16)) = w;
-        }
-        fence_proxy_async_smem();
-        tc_fence_before_sync();
-        mbar_arrive(&p_full[h]);
-      }
-    }
-    // Epilogue: O / l -> bf16 rows.
-    for (int h = 0; h < NH && ok; ++h) {
-      ok = warp_wait(&o_done[h], (n_kv - 1) & 1, abort_flag);
+      ok = warp_wait(&s_full[h], jt & 1, abort_flag);
       if (!ok) break;
       tc_fence_after_sync();
-      const float inv = 1.f / l_run[h];
+      float sv[BN / 32][32];
+#pragma unroll
+      for (int hh = 0; hh < BN / 32; ++hh)
+        tmem_load32(tmem + lane_base + kSCol + h * BN + hh * 32, sv[hh]);
+      // Tile max of the scaled logits over this row's visible keys.
+      const bool full_row = key0 + BN - 1 <= key_limit;
+      float mt;
+      if (qs >= 0.f) {
+        float mx = -INFINITY;
+        if (full_row) {
+#pragma unroll
+          for (int i = 0; i < BN; ++i) mx = fmaxf(mx, sv[i / 32][i % 32]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < BN; ++i)
+            if (key0 + i <= key_limit) mx = fmaxf(mx, sv[i / 32][i % 32]);
+        }
+        mt = mx * qs;
+      } else {
+        float mn = INFINITY;
+#pragma unroll
+        for (int i = 0; i < BN; ++i)
+          if (key0 + i <= key_limit) mn = fminf(mn, sv[i / 32][i % 32]);
+        mt = mn * qs;
+      }
+      // Key 0 is visible to every row, so the first tile sets a finite max.
+      float alpha = 1.f;
+      const bool raise = (jt == 0) || (mt > m_ref + 8.f);
+      if (raise) {
+        const float m_new = fmaxf(m_ref, mt);
+        alpha = fast_exp2(m_ref - m_new);  // 0 on the first tile
+        m_ref = m_new;
+      }
+      float rs = 0.f;
+      if (full_row) {
+#pragma unroll
+        for (int i = 0; i < BN; ++i) {
+          const float e = fast_exp2(fmaf(sv[i / 32][i % 32], qs, -m_ref));
+          sv[i / 32][i % 32] = e;
+          rs += e;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < BN; ++i) {
+          const float e = (key0 + i <= key_limit) ? fast_exp2(fmaf(sv[i / 32][i % 32], qs, -m_ref)) : 0.f;
+          sv[i / 32][i % 32] = e;
+          rs += e;
+        }
+      }
+      if (jt > 0) {
+        // PV of the previous tile must be complete: O may be rescaled, P reused.
+        ok = warp_wait(&o_done[h], (jt - 1) & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after_sync();
+        if (__any_sync(0xffffffffu, alpha < 1.f)) {
+#pragma unroll 1
+          for (int cc = 0; cc < D / 32; ++cc) {
+            float ov[32];
+            const uint32_t oa = tmem + lane_base + kOCol + h * D + cc * 32;
+            tmem_load32(oa, ov);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] *= alpha;
+            tmem_store32(oa, ov);
+          }
+        }
+      }
+      l_run = l_run * alpha + rs;
+      if (h == 0 && jt == n_kv - 1 && key0 + BN > len_k) {
+        // Keys past the context may hold stale bits (even NaN); P is zero
+        // there, but 0 * NaN is not, so clear those V rows first.  (The MMA
+        // thread issues every head's last P.V after this warpgroup's arrival.)
+        ok = warp_wait(&v_full[jt % kStages], (jt / kStages) & 1, abort_flag);
+        if (!ok) break;
+        const int first = len_k - key0;
+        uint8_t *vt = sV + (jt % kStages) * L::kKVBytes;
+        const int nchunks = (BN - first) * 8 * XR;  // 16-byte chunks to clear
+        for (int i = row; i < nchunks; i += 128) {
+          const int x = i / ((BN - first) * 8);
+          const int rem = i - x * (BN - first) * 8;
+          const int rr = first + rem / 8;
+          *reinterpret_cast<uint4 *>(vt + x * BN * 128 + rr * 128 + (rem & 7) * 16) =
+              make_uint4(0, 0, 0, 0);
+        }
+      }
+      // P (bf16) into the 128B-swizzled K-major tile: row `row`, 16-byte chunk c
+      // of keys 8c..8c+7 lands at chunk c ^ (row & 7).
+      uint8_t *prow = sP + h * L::kPBytes + row * 128;
+#pragma unroll
+      for (int cidx = 0; cidx < BN / 8; ++cidx) {
+        uint4 w;
+        const float *pv = &sv[cidx / 4][(cidx % 4) * 8];
+        w.x = pack_bf16x2(pv[0], pv[1]);
+        w.y = pack_bf16x2(pv[2], pv[3]);
+        w.z = pack_bf16x2(pv[4], pv[5]);
+        w.w = pack_bf16x2(pv[6], pv[7]);
+        *reinterpret_cast<uint4 *>(prow + ((cidx ^ (row & 7)) * 16)) = w;
+      }
+      fence_proxy_async_smem();
+      tc_fence_before_sync();
+      mbar_arrive(&p_full[h]);
+    }
+    // Epilogue: O / l -> bf16 rows.
+    if (ok) ok = warp_wait(&o_done[h], (n_kv - 1) & 1, abort_flag);
+    if (ok) {
+      tc_fence_after_sync();
+      const float inv = 1.f / l_run;
       uint16_t *dst = p.out + ((int64_t)(q_begin + q0 + row) * p.num_q_heads + h_first + h) * D;
 #pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
@@ -426,7 +459,7 @@ pkv_status launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const CU
   }
   const int64_t grid = (int64_t)prm.q_tiles * prm.num_seqs * (prm.num_q_heads / NH);
   if (grid > 0x7FFFFFFFLL) return PKV_ERR_INVALID_ARG;
-  paged_prefill_kernel<D, NH><<<(unsigned)grid, kThreads, smem, stream>>>(tq, tk, tv, prm);
+  paged_prefill_kernel<D, NH><<<(unsigned)grid, threads_for<NH>(), smem, stream>>>(tq, tk, tv, prm);
   return launch_status();
 }
 
