@@ -33,10 +33,16 @@ namespace {
 
 constexpr int BM = 128;  // query rows per tile (MMA M)
 constexpr int BN = 64;   // keys per tile
-constexpr int kStages = 4;  // K/V ring depth (fills shared memory for D=128, 2 heads)
-// Warp 0: TMA producer; warp 1: MMA issuer; then one 4-warp softmax group per head.
+// Ring depths.  A K slot is held until its S MMAs finish, a V slot until its
+// P.V has run; the rings turn over independently.  8 slots fill shared memory
+// for D=128 with 2 heads (measured: the split 4/4, 3/5 or 2/6 makes no
+// difference; the fill rate of the rings is the limit).
+constexpr int kKStages = 4;
+constexpr int kVStages = 4;
+// Warp 0: Q/K TMA producer; warp 1: MMA issuer; then one 4-warp softmax group
+// per head; last: V TMA producer.
 template <int NH>
-constexpr int threads_for() { return 64 + 128 * NH; }
+constexpr int threads_for() { return 96 + 128 * NH; }
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct PrefillParams {
@@ -63,17 +69,20 @@ struct PrefillLayout {
   static constexpr int kPBytes = BM * BN * 2;  // one head's P tile
   static constexpr int q = 0;
   static constexpr int k = q + NH * kQBytes;
-  static constexpr int v = k + kStages * kKVBytes;
-  static constexpr int p = v + kStages * kKVBytes;
+  static constexpr int v = k + kKStages * kKVBytes;
+  static constexpr int p = v + kVStages * kKVBytes;
   static constexpr int bars = p + NH * kPBytes;
-  // barriers: q_full, k_full[S], v_full[S], kv_empty[S], s_full[NH], p_full[NH], o_done[NH], drain
-  static constexpr int kNumBars = 1 + 3 * kStages + 3 * NH + 1;
+  // barriers: q_full, k_full[SK], v_full[SV], k_empty[SK], v_empty[SV],
+  // s_full[NH][2], p_full[NH], o_done[NH], drain
+  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 * NH + 2 * NH + 1;
   static constexpr int misc = bars + kNumBars * 8;  // tmem address, abort flag
   static constexpr int total = misc + 16;
-  static constexpr int kTmemCols = NH * (BN + D) <= 128 ? 128 : (NH * (BN + D) <= 256 ? 256 : 512);
+  static constexpr int kCols = NH * D + 2 * NH * BN;  // O per head + two S buffers per head
+  static constexpr int kTmemCols = kCols <= 128 ? 128 : (kCols <= 256 ? 256 : 512);
 };
 
-// Tensor-memory columns: O_h at kOCol + h*D, S_h at kSCol + h*BN (fp32, lane = row).
+// Tensor-memory columns (fp32, lane = query row): O_h at kO + h*D; the two S
+// buffers of head h at kS + (2h + b)*BN, b = tile index & 1.
 template <int D, int NH>
 struct TmemCols {
   static constexpr uint32_t kO = 0;
@@ -94,6 +103,7 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
   constexpr int XR = D / 64;  // 128-byte swizzle regions across D
   constexpr uint32_t kOCol = TmemCols<D, NH>::kO;
   constexpr uint32_t kSCol = TmemCols<D, NH>::kS;
+  constexpr int kVWarp = 2 + 4 * NH;  // V producer warp (after the softmax warpgroups)
 
   // ---- which tile -------------------------------------------------------
   // Sequence-major order, each sequence's heaviest q tiles first, head groups
@@ -137,10 +147,11 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::bars);
   uint64_t *q_full = bars;
   uint64_t *k_full = bars + 1;
-  uint64_t *v_full = k_full + kStages;
-  uint64_t *kv_empty = v_full + kStages;
-  uint64_t *s_full = kv_empty + kStages;
-  uint64_t *p_full = s_full + NH;
+  uint64_t *v_full = k_full + kKStages;
+  uint64_t *k_empty = v_full + kVStages;
+  uint64_t *v_empty = k_empty + kKStages;
+  uint64_t *s_full = v_empty + kVStages;  // [NH][2]
+  uint64_t *p_full = s_full + 2 * NH;
   uint64_t *o_done = p_full + NH;
   uint64_t *drain = o_done + NH;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::misc);
@@ -151,13 +162,17 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < kKStages; ++i) {
       mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+    }
+    for (int i = 0; i < kVStages; ++i) {
       mbar_init(&v_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
+      mbar_init(&v_empty[i], 1);
     }
     for (int h = 0; h < NH; ++h) {
-      mbar_init(&s_full[h], 1);
+      mbar_init(&s_full[2 * h], 1);
+      mbar_init(&s_full[2 * h + 1], 1);
       mbar_init(&p_full[h], 128);  // one softmax warpgroup per head
       mbar_init(&o_done[h], 1);
     }
@@ -174,47 +189,59 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    // ================= TMA producer =================
+  // Physical block and in-block offset of KV tile jt (bounds-checked).
+  auto block_of = [&](int jt, int &off) {
+    const int key0 = jt * BN;
+    const int lb = key0 / p.block_size;
+    off = key0 - lb * p.block_size;
+    int blk = p.block_tables[(int64_t)s * p.max_blocks_per_seq + lb];
+    if (blk < 0 || (int64_t)blk >= p.num_blocks) {
+      flag_status(p.status, PKV_DEV_BAD_BLOCK);
+      blk = 0;
+    }
+    return blk;
+  };
+
+  if (warp == 0 || warp == kVWarp) {
+    // ============ TMA producers: warp 0 loads Q and K, the last warp V ============
+    // The K and V rings turn over independently: a K slot is free once the
+    // S MMAs that read it are done, a V slot once its P.V MMAs are done.
     if (lane == 0) {
-      tma_prefetch_map(&tm_q);
-      tma_prefetch_map(&tm_k);
-      tma_prefetch_map(&tm_v);
-      mbar_arrive_expect_tx(q_full, NH * L::kQBytes);
-      for (int h = 0; h < NH; ++h)
-        for (int x = 0; x < XR; ++x)
-          tma_load_3d(sQ + h * L::kQBytes + x * BM * 128, &tm_q, q_full, x * 64, h_first + h,
-                      q_begin + q0);
+      const bool is_k = (warp == 0);
+      uint64_t *full = is_k ? k_full : v_full;
+      uint64_t *empty = is_k ? k_empty : v_empty;
+      uint8_t *ring = is_k ? sK : sV;
+      const CUtensorMap *map = is_k ? &tm_k : &tm_v;
+      const int nst = is_k ? kKStages : kVStages;
+      if (is_k) {
+        tma_prefetch_map(&tm_q);
+        tma_prefetch_map(&tm_k);
+        mbar_arrive_expect_tx(q_full, NH * L::kQBytes);
+        for (int h = 0; h < NH; ++h)
+          for (int x = 0; x < XR; ++x)
+            tma_load_3d(sQ + h * L::kQBytes + x * BM * 128, &tm_q, q_full, x * 64, h_first + h,
+                        q_begin + q0);
+      } else {
+        tma_prefetch_map(&tm_v);
+      }
       int issued = 0;
       for (int jt = 0; jt < n_kv; ++jt) {
-        const int st = jt % kStages;
-        if (jt >= kStages &&
-            !mbar_wait_bounded(&kv_empty[st], ((jt / kStages) - 1) & 1, abort_flag))
+        const int st = jt % nst;
+        if (jt >= nst && !mbar_wait_bounded(&empty[st], ((jt / nst) - 1) & 1, abort_flag))
           break;
-        const int key0 = jt * BN;
-        const int lb = key0 / p.block_size;
-        const int off = key0 - lb * p.block_size;
-        int blk = p.block_tables[(int64_t)s * p.max_blocks_per_seq + lb];
-        if (blk < 0 || (int64_t)blk >= p.num_blocks) {
-          flag_status(p.status, PKV_DEV_BAD_BLOCK);
-          blk = 0;
-        }
-        mbar_arrive_expect_tx(&k_full[st], L::kKVBytes);
+        int off;
+        const int blk = block_of(jt, off);
+        mbar_arrive_expect_tx(&full[st], L::kKVBytes);
         for (int x = 0; x < XR; ++x)
-          tma_load_4d(sK + st * L::kKVBytes + x * BN * 128, &tm_k, &k_full[st], x * 64, kvh, off,
-                      blk);
-        mbar_arrive_expect_tx(&v_full[st], L::kKVBytes);
-        for (int x = 0; x < XR; ++x)
-          tma_load_4d(sV + st * L::kKVBytes + x * BN * 128, &tm_v, &v_full[st], x * 64, kvh, off,
+          tma_load_4d(ring + st * L::kKVBytes + x * BN * 128, map, &full[st], x * 64, kvh, off,
                       blk);
         issued = jt + 1;
       }
       // Do not leave while copies into this CTA's shared memory are in flight.
-      if (!mbar_wait_bounded(q_full, 0, nullptr)) flag_status(p.status, PKV_DEV_TIMEOUT);
-      for (int i = max(0, issued - kStages); i < issued; ++i) {
-        if (!mbar_wait_bounded(&k_full[i % kStages], (i / kStages) & 1, nullptr)) flag_status(p.status, PKV_DEV_TIMEOUT);
-        if (!mbar_wait_bounded(&v_full[i % kStages], (i / kStages) & 1, nullptr)) flag_status(p.status, PKV_DEV_TIMEOUT);
-      }
+      if (is_k && !mbar_wait_bounded(q_full, 0, nullptr)) flag_status(p.status, PKV_DEV_TIMEOUT);
+      for (int i = max(0, issued - nst); i < issued; ++i)
+        if (!mbar_wait_bounded(&full[i % nst], (i / nst) & 1, nullptr))
+          flag_status(p.status, PKV_DEV_TIMEOUT);
     }
   } else if (warp == 1) {
     // ================= MMA issuer =================
@@ -228,7 +255,7 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
       bool ok = mbar_wait_bounded(q_full, 0, abort_flag);
       tc_fence_after_sync();
       auto issue_pv = [&](int jt, int h) {
-        const int pst = jt % kStages;
+        const int pst = jt % kVStages;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
           const uint64_t a = umma_desc_sw128(p_addr + h * L::kPBytes + kk * 32, 16, 1024);
@@ -238,17 +265,31 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
         }
         umma_commit(&o_done[h]);
       };
+      // P.V of tile jt-1 for every head, in head order, once V(jt-1) and that
+      // head's P are ready; then its V slot is released.  Head order also
+      // keeps every head's last P.V behind warpgroup 0, which clears the V
+      // rows past the context before it publishes its P.
+      auto pv_step = [&](int jt) {
+        bool good = mbar_wait_bounded(&v_full[jt % kVStages], (jt / kVStages) & 1, abort_flag);
+        for (int h = 0; h < NH && good; ++h) {
+          good = mbar_wait_bounded(&p_full[h], jt & 1, abort_flag);
+          if (!good) break;
+          tc_fence_after_sync();
+          issue_pv(jt, h);
+        }
+        if (good) umma_commit(&v_empty[jt % kVStages]);
+        return good;
+      };
+      // Per tile jt: S_h(jt) for every head into S buffer jt & 1 (free: the
+      // softmax of tile jt-2 was waited for before P.V(jt-2) was issued), then
+      // P.V(jt-1).  S of the next tile is computed while this tile's softmax
+      // runs.
       for (int jt = 0; jt < n_kv && ok; ++jt) {
-        const int st = jt % kStages;
-        ok = mbar_wait_bounded(&k_full[st], (jt / kStages) & 1, abort_flag);
+        const int st = jt % kKStages;
+        ok = mbar_wait_bounded(&k_full[st], (jt / kKStages) & 1, abort_flag);
         if (!ok) break;
         tc_fence_after_sync();
-        for (int h = 0; h < NH && ok; ++h) {
-          if (jt > 0) {
-            ok = mbar_wait_bounded(&p_full[h], (jt - 1) & 1, abort_flag);
-            if (!ok) break;
-            tc_fence_after_sync();
-          }
+        for (int h = 0; h < NH; ++h) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk & 3) * 32;
@@ -256,31 +297,14 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
                 umma_desc_sw128(q_addr + h * L::kQBytes + (kk / 4) * BM * 128 + off, 16, 1024);
             const uint64_t b =
                 umma_desc_sw128(k_addr + st * L::kKVBytes + (kk / 4) * BN * 128 + off, 16, 1024);
-            umma_bf16(tmem + kSCol + h * BN, a, b, idesc_s, kk > 0 ? 1u : 0u);
+            umma_bf16(tmem + kSCol + (2 * h + (jt & 1)) * BN, a, b, idesc_s, kk > 0 ? 1u : 0u);
           }
-          umma_commit(&s_full[h]);
-          if (jt > 0) {
-            if (h == 0) {
-              ok = mbar_wait_bounded(&v_full[(jt - 1) % kStages], ((jt - 1) / kStages) & 1,
-                                     abort_flag);
-              if (!ok) break;
-              tc_fence_after_sync();
-            }
-            issue_pv(jt - 1, h);
-          }
+          umma_commit(&s_full[2 * h + (jt & 1)]);
         }
-        if (ok && jt > 0) umma_commit(&kv_empty[(jt - 1) % kStages]);
+        umma_commit(&k_empty[st]);
+        if (jt > 0) ok = pv_step(jt - 1);
       }
-      if (ok) {
-        const int last = n_kv - 1;
-        ok = mbar_wait_bounded(&v_full[last % kStages], (last / kStages) & 1, abort_flag);
-        for (int h = 0; h < NH && ok; ++h) {
-          ok = mbar_wait_bounded(&p_full[h], last & 1, abort_flag);
-          if (!ok) break;
-          tc_fence_after_sync();
-          issue_pv(last, h);
-        }
-      }
+      if (ok) ok = pv_step(n_kv - 1);
       // Wait for every MMA this thread issued before tensor memory is freed.
       umma_commit(drain);
       if (!mbar_wait_bounded(drain, 0, nullptr)) flag_status(p.status, PKV_DEV_TIMEOUT);
@@ -301,60 +325,81 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
     bool ok = true;
     for (int jt = 0; jt < n_kv && ok; ++jt) {
       const int key0 = jt * BN;
-      ok = warp_wait(&s_full[h], jt & 1, abort_flag);
+      ok = warp_wait(&s_full[2 * h + (jt & 1)], (jt >> 1) & 1, abort_flag);
       if (!ok) break;
       tc_fence_after_sync();
-      float sv[BN / 32][32];
-#pragma unroll
-      for (int hh = 0; hh < BN / 32; ++hh)
-        tmem_load32(tmem + lane_base + kSCol + h * BN + hh * 32, sv[hh]);
-      // Tile max of the scaled logits over this row's visible keys.
+      float sv[BN];
+      static_assert(BN == 64, "S is read with one 64-column TMEM load");
+      tmem_load64(tmem + lane_base + kSCol + (2 * h + (jt & 1)) * BN, sv);
+      // Tile max of the scaled logits over this row's visible keys (4-way tree).
       const bool full_row = key0 + BN - 1 <= key_limit;
       float mt;
-      if (qs >= 0.f) {
-        float mx = -INFINITY;
-        if (full_row) {
+      {
+        float e0 = -INFINITY, e1 = -INFINITY, e2 = -INFINITY, e3 = -INFINITY;
+        if (qs >= 0.f) {
+          if (full_row) {
 #pragma unroll
-          for (int i = 0; i < BN; ++i) mx = fmaxf(mx, sv[i / 32][i % 32]);
+            for (int i = 0; i < BN; i += 4) {
+              e0 = fmaxf(e0, sv[i]);
+              e1 = fmaxf(e1, sv[i + 1]);
+              e2 = fmaxf(e2, sv[i + 2]);
+              e3 = fmaxf(e3, sv[i + 3]);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < BN; ++i)
+              if (key0 + i <= key_limit) e0 = fmaxf(e0, sv[i]);
+          }
+          mt = fmaxf(fmaxf(e0, e1), fmaxf(e2, e3)) * qs;
         } else {
+          e0 = INFINITY;
 #pragma unroll
           for (int i = 0; i < BN; ++i)
-            if (key0 + i <= key_limit) mx = fmaxf(mx, sv[i / 32][i % 32]);
+            if (key0 + i <= key_limit) e0 = fminf(e0, sv[i]);
+          mt = e0 * qs;
         }
-        mt = mx * qs;
-      } else {
-        float mn = INFINITY;
-#pragma unroll
-        for (int i = 0; i < BN; ++i)
-          if (key0 + i <= key_limit) mn = fminf(mn, sv[i / 32][i % 32]);
-        mt = mn * qs;
       }
-      // Key 0 is visible to every row, so the first tile sets a finite max.
+      // Key 0 is in the first tile and visible to every row, so the first tile
+      // sets a finite max (the -inf guard keeps a row with no visible key at
+      // alpha = 0 instead of NaN).
       float alpha = 1.f;
-      const bool raise = (jt == 0) || (mt > m_ref + 8.f);
-      if (raise) {
+      if (jt == 0 || mt > m_ref + 8.f) {
         const float m_new = fmaxf(m_ref, mt);
-        alpha = fast_exp2(m_ref - m_new);  // 0 on the first tile
+        alpha = (m_ref == -INFINITY) ? 0.f : fast_exp2(m_ref - m_new);
         m_ref = m_new;
       }
-      float rs = 0.f;
-      if (full_row) {
+      float rs;
+      {
+        float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
+        if (full_row) {
 #pragma unroll
-        for (int i = 0; i < BN; ++i) {
-          const float e = fast_exp2(fmaf(sv[i / 32][i % 32], qs, -m_ref));
-          sv[i / 32][i % 32] = e;
-          rs += e;
-        }
-      } else {
+          for (int i = 0; i < BN; i += 4) {
+            sv[i] = fast_exp2(fmaf(sv[i], qs, -m_ref));
+            sv[i + 1] = fast_exp2(fmaf(sv[i + 1], qs, -m_ref));
+            sv[i + 2] = fast_exp2(fmaf(sv[i + 2], qs, -m_ref));
+            sv[i + 3] = fast_exp2(fmaf(sv[i + 3], qs, -m_ref));
+            r0 += sv[i];
+            r1 += sv[i + 1];
+            r2 += sv[i + 2];
+            r3 += sv[i + 3];
+          }
+        } else {
 #pragma unroll
-        for (int i = 0; i < BN; ++i) {
-          const float e = (key0 + i <= key_limit) ? fast_exp2(fmaf(sv[i / 32][i % 32], qs, -m_ref)) : 0.f;
-          sv[i / 32][i % 32] = e;
-          rs += e;
+          for (int i = 0; i < BN; i += 4) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              sv[i + u] =
+                  (key0 + i + u <= key_limit) ? fast_exp2(fmaf(sv[i + u], qs, -m_ref)) : 0.f;
+            r0 += sv[i];
+            r1 += sv[i + 1];
+            r2 += sv[i + 2];
+            r3 += sv[i + 3];
+          }
         }
+        rs = (r0 + r1) + (r2 + r3);
       }
       if (jt > 0) {
-        // PV of the previous tile must be complete: O may be rescaled, P reused.
+        // P.V of the previous tile must be complete: O may be rescaled, P reused.
         ok = warp_wait(&o_done[h], (jt - 1) & 1, abort_flag);
         if (!ok) break;
         tc_fence_after_sync();
@@ -371,14 +416,14 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
         }
       }
       l_run = l_run * alpha + rs;
-      if (h == 0 && jt == n_kv - 1 && key0 + BN > len_k) {
+      if (h == 0 && key0 + BN > len_k) {
         // Keys past the context may hold stale bits (even NaN); P is zero
         // there, but 0 * NaN is not, so clear those V rows first.  (The MMA
         // thread issues every head's last P.V after this warpgroup's arrival.)
-        ok = warp_wait(&v_full[jt % kStages], (jt / kStages) & 1, abort_flag);
+        ok = warp_wait(&v_full[jt % kVStages], (jt / kVStages) & 1, abort_flag);
         if (!ok) break;
         const int first = len_k - key0;
-        uint8_t *vt = sV + (jt % kStages) * L::kKVBytes;
+        uint8_t *vt = sV + (jt % kVStages) * L::kKVBytes;
         const int nchunks = (BN - first) * 8 * XR;  // 16-byte chunks to clear
         for (int i = row; i < nchunks; i += 128) {
           const int x = i / ((BN - first) * 8);
@@ -394,7 +439,7 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
 #pragma unroll
       for (int cidx = 0; cidx < BN / 8; ++cidx) {
         uint4 w;
-        const float *pv = &sv[cidx / 4][(cidx % 4) * 8];
+        const float *pv = &sv[cidx * 8];
         w.x = pack_bf16x2(pv[0], pv[1]);
         w.y = pack_bf16x2(pv[2], pv[3]);
         w.z = pack_bf16x2(pv[4], pv[5]);
