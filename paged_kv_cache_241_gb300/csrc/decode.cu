@@ -38,7 +38,9 @@ namespace {
 constexpr int kTile = 64;           // tokens per TMA tile
 constexpr int kConsumerWarps = 4;   // compute warps per CTA
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStages = 4;          // shared-memory tile ring
+// Shared-memory tile ring depth: 4 stages, 3 for groups of 4+ query heads so
+// that three CTAs still fit on an SM.
+__host__ __device__ constexpr int decode_stages(int G) { return G >= 4 ? 3 : 4; }
 constexpr int kMaxSeqs = 16384;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -150,22 +152,17 @@ __device__ __forceinline__ int octet_base(int r) {
   }
 }
 
+// The G probability pairs of one token (16-byte vector loads where possible).
 template <int G>
-__device__ __forceinline__ void load_probs(const float *p, float (&pv)[G]) {
+__device__ __forceinline__ void load_prob_pairs(const float2 *p, float2 (&pv)[G]) {
   if constexpr (G == 1) {
     pv[0] = p[0];
-  } else if constexpr (G == 2) {
-    const float2 a = *reinterpret_cast<const float2 *>(p);
-    pv[0] = a.x;
-    pv[1] = a.y;
   } else {
 #pragma unroll
-    for (int i = 0; i < G; i += 4) {
+    for (int i = 0; i < G; i += 2) {
       const float4 a = *reinterpret_cast<const float4 *>(p + i);
-      pv[i] = a.x;
-      pv[i + 1] = a.y;
-      pv[i + 2] = a.z;
-      pv[i + 3] = a.w;
+      pv[i] = make_float2(a.x, a.y);
+      pv[i + 1] = make_float2(a.z, a.w);
     }
   }
 }
@@ -175,10 +172,11 @@ struct DecodeSmem {
   int tiles, qbuf, bars, logits, red, stats, misc, prefix, ctx, total;
   __host__ __device__ DecodeSmem(int D, int G, int bs, int num_seqs) {
     tiles = 0;
-    qbuf = tiles + kStages * kTile * D * 2;  // [2][G*D] bf16: q of the next items
-    bars = qbuf + 2 * G * D * 2;             // full[S], empty[S], q_full[2], q_empty[2]
-    logits = bars + (2 * kStages + 4) * 8;
-    red = logits + ((bs * G * 4 + 15) & ~15);
+    const int stages = decode_stages(G);
+    qbuf = tiles + stages * kTile * D * 2;  // [2][G*D] bf16: q of the next items
+    bars = qbuf + 2 * G * D * 2;            // full[S], empty[S], q_full[2], q_empty[2]
+    logits = bars + (2 * stages + 4) * 8;   // [block_size][G] float pairs
+    red = logits + ((bs * G * 8 + 15) & ~15);
     stats = red + kConsumerWarps * G * D * 4;
     misc = stats + 2 * G * 4;
     prefix = misc + 16;
@@ -201,6 +199,7 @@ template <int D, int G>
 __global__ void __launch_bounds__(kThreads)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
+  constexpr int kStages = decode_stages(G);
   constexpr int kTileBytes = kTile * D * 2;
   constexpr int kQBytes = G * D * 2;
   constexpr int CPL = D / 64;  // 16-byte chunks per lane per token (phase 1)
@@ -217,7 +216,9 @@ __global__ void __launch_bounds__(kThreads)
   uint64_t *empty = full + kStages;
   uint64_t *q_full = empty + kStages;
   uint64_t *q_empty = q_full + 2;
-  float *logits = reinterpret_cast<float *>(smem + lay.logits);  // [block_size][G]
+  // Per token and head: phase 1 stores the logit in .x, phase 2 replaces the
+  // pair by (p, p) so phase 3 can feed it straight to a packed FMA.
+  float2 *logits = reinterpret_cast<float2 *>(smem + lay.logits);  // [block_size][G]
   float *red = reinterpret_cast<float *>(smem + lay.red);        // [warps][G][D]
   float *mstat = reinterpret_cast<float *>(smem + lay.stats);    // [G]
   float *lstat = mstat + G;                                      // [G]
@@ -392,8 +393,9 @@ __global__ void __launch_bounds__(kThreads)
     const int nblk = prefix[s + 1] - prefix[s];
     const int h0 = j * G;
 
-    // q fragment from the staged copy: dims of chunks r + 8c, in log2 units.
-    float qf[G][CPL * 8];
+    // q fragment from the staged copy: dim pairs (2e, 2e+1) of chunks r + 8c,
+    // in log2 units.
+    float2 qf[G][CPL * 4];
     {
       const int qb = item_no & 1;
       const bool ok = mbar_wait_bounded(&q_full[qb], (item_no >> 1) & 1, abort_flag);
@@ -406,10 +408,8 @@ __global__ void __launch_bounds__(kThreads)
           if (ok) raw = *reinterpret_cast<const uint4 *>(qs + h * D + (r + 8 * c) * 8);
           const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            qf[h][c * 8 + 2 * e] = bf16lo(wv[e]) * p.qscale;
-            qf[h][c * 8 + 2 * e + 1] = bf16hi(wv[e]) * p.qscale;
-          }
+          for (int e = 0; e < 4; ++e)
+            qf[h][c * 4 + e] = make_float2(bf16lo(wv[e]) * p.qscale, bf16hi(wv[e]) * p.qscale);
         }
       }
       __syncwarp();
@@ -423,9 +423,10 @@ __global__ void __launch_bounds__(kThreads)
       if (ok) {
         const uint16_t *tile = reinterpret_cast<const uint16_t *>(tiles + st * kTileBytes);
         const int tok0 = warp * 16 + gid * 4;
-        float acc[NV];
+        // Packed FP32x2 FMAs: even and odd dims accumulate in the two halves.
+        float2 acc2[NV];
 #pragma unroll
-        for (int i = 0; i < NV; ++i) acc[i] = 0.f;
+        for (int i = 0; i < NV; ++i) acc2[i] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const uint16_t *krow = tile + (tok0 + i) * D;
@@ -435,16 +436,16 @@ __global__ void __launch_bounds__(kThreads)
             const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float k0 = bf16lo(wv[e]);
-              const float k1 = bf16hi(wv[e]);
+              const float2 kk = make_float2(bf16lo(wv[e]), bf16hi(wv[e]));
 #pragma unroll
-              for (int h = 0; h < G; ++h) {
-                acc[i * G + h] = fmaf(qf[h][c * 8 + 2 * e], k0, acc[i * G + h]);
-                acc[i * G + h] = fmaf(qf[h][c * 8 + 2 * e + 1], k1, acc[i * G + h]);
-              }
+              for (int h = 0; h < G; ++h)
+                acc2[i * G + h] = __ffma2_rn(qf[h][c * 4 + e], kk, acc2[i * G + h]);
             }
           }
         }
+        float acc[NV];
+#pragma unroll
+        for (int i = 0; i < NV; ++i) acc[i] = acc2[i].x + acc2[i].y;
         octet_reduce<NV>(acc, r);
         const int base = octet_base<NV>(r);
         constexpr int kOwned = NV >= 8 ? NV / 8 : 1;
@@ -454,7 +455,7 @@ __global__ void __launch_bounds__(kThreads)
             const int vi = base + u;
             const int i = vi / G;
             const int h = vi - i * G;
-            logits[(t * kTile + tok0 + i) * G + h] = acc[u];
+            logits[(t * kTile + tok0 + i) * G + h].x = acc[u];
           }
         }
       }
@@ -466,12 +467,12 @@ __global__ void __launch_bounds__(kThreads)
     // Phase 2: exact softmax statistics of this item, per head.
     for (int h = warp; h < G; h += kConsumerWarps) {
       float m = -INFINITY;
-      for (int x = lane; x < valid; x += 32) m = fmaxf(m, logits[x * G + h]);
+      for (int x = lane; x < valid; x += 32) m = fmaxf(m, logits[x * G + h].x);
       m = warp_max(m);
       float l = 0.f;
       for (int x = lane; x < valid; x += 32) {
-        const float e = fast_exp2(logits[x * G + h] - m);
-        logits[x * G + h] = e;
+        const float e = fast_exp2(logits[x * G + h].x - m);
+        logits[x * G + h] = make_float2(e, e);
         l += e;
       }
       l = warp_sum(l);
@@ -483,11 +484,11 @@ __global__ void __launch_bounds__(kThreads)
     named_bar_sync(1, kConsumerWarps * 32);
 
     // Phase 3: unnormalised P.V, lane owns dims [lane*DPL, lane*DPL + DPL).
-    float acc_o[G][DPL];
+    float2 acc_o[G][DPL / 2];
 #pragma unroll
     for (int h = 0; h < G; ++h)
 #pragma unroll
-      for (int e = 0; e < DPL; ++e) acc_o[h][e] = 0.f;
+      for (int e = 0; e < DPL / 2; ++e) acc_o[h][e] = make_float2(0.f, 0.f);
     for (int t = 0; t < ntile; ++t, ++ctile) {
       const int st = ctile % kStages;
       const bool ok = mbar_wait_bounded(&full[st], (ctile / kStages) & 1, abort_flag);
@@ -497,24 +498,21 @@ __global__ void __launch_bounds__(kThreads)
         const int thi = min(tlo + 16, valid - t * kTile);
 #pragma unroll 4
         for (int tok = tlo; tok < thi; ++tok) {
-          float vf[DPL];
+          float2 vf[DPL / 2];
           if constexpr (DPL == 4) {
             const uint2 raw = *reinterpret_cast<const uint2 *>(tile + tok * D + lane * 4);
-            vf[0] = bf16lo(raw.x);
-            vf[1] = bf16hi(raw.x);
-            vf[2] = bf16lo(raw.y);
-            vf[3] = bf16hi(raw.y);
+            vf[0] = make_float2(bf16lo(raw.x), bf16hi(raw.x));
+            vf[1] = make_float2(bf16lo(raw.y), bf16hi(raw.y));
           } else {
             const uint32_t raw = *reinterpret_cast<const uint32_t *>(tile + tok * D + lane * 2);
-            vf[0] = bf16lo(raw);
-            vf[1] = bf16hi(raw);
+            vf[0] = make_float2(bf16lo(raw), bf16hi(raw));
           }
-          float pv[G];
-          load_probs<G>(logits + (t * kTile + tok) * G, pv);
+          float2 pv[G];
+          load_prob_pairs<G>(logits + (t * kTile + tok) * G, pv);
 #pragma unroll
           for (int h = 0; h < G; ++h)
 #pragma unroll
-            for (int e = 0; e < DPL; ++e) acc_o[h][e] = fmaf(pv[h], vf[e], acc_o[h][e]);
+            for (int e = 0; e < DPL / 2; ++e) acc_o[h][e] = __ffma2_rn(pv[h], vf[e], acc_o[h][e]);
         }
       }
       __syncwarp();
@@ -525,7 +523,8 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
     for (int h = 0; h < G; ++h)
 #pragma unroll
-      for (int e = 0; e < DPL; ++e) red[(warp * G + h) * D + lane * DPL + e] = acc_o[h][e];
+      for (int e = 0; e < DPL / 2; ++e)
+        *reinterpret_cast<float2 *>(red + (warp * G + h) * D + lane * DPL + 2 * e) = acc_o[h][e];
     named_bar_sync(1, kConsumerWarps * 32);
     if (nblk == 1) {
       for (int idx = tid; idx < G * D / 2; idx += kConsumerWarps * 32) {
