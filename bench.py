@@ -81,6 +81,28 @@ def prefill_bytes(b):
     return kv + 2 * int(b.q.shape[0]) * b.num_q_heads * b.head_dim * 2
 
 
+# ------------------------------------------------------------ ncu counters
+
+def ncu_traffic(kernel):
+    """DRAM bytes per launch (read + write) of `kernel` from the committed ncu
+    summary, or None when there is none or the kernel's sources changed since
+    the counters were taken (source hash recorded beside them)."""
+    import hashlib
+
+    try:
+        with open(os.path.join(ROOT, "profiles", "counters.json")) as f:
+            rec = json.load(f)[kernel]
+        h = hashlib.sha256()
+        for src in rec["sources"]:
+            with open(os.path.join(ROOT, "paged_kv_cache_241_gb300", src), "rb") as g:
+                h.update(g.read())
+        if h.hexdigest()[:16] != rec["source_sha256_16"]:
+            return None
+        return int(rec["dram_read_bytes"]) + int(rec["dram_write_bytes"])
+    except Exception:
+        return None
+
+
 # ------------------------------------------------------------ clock sampling
 
 class ClockSampler:
@@ -454,7 +476,9 @@ def main():
                 rec["tflops"] = tf
                 rec["roofline"] = {"bound": "tensor", "achieved": tf,
                                    "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                                   "frac": tf / peaks["bf16_tflops"]}
+                                   "frac": tf / peaks["bf16_tflops"],
+                                   "traffic": ncu_traffic("paged_prefill_kernel<128,2>")
+                                   if name == "prefill" else None}
                 kvb = store_bytes(bb) / (sm_ * 1e-3) / 1e9
                 rec["kv_store"] = {"GB/s": kvb, "frac": kvb / peaks["hbm_gbs"],
                                    "bytes": store_bytes(bb)}
@@ -480,7 +504,8 @@ def main():
                    "l2": "4 rotating cache copies (4.3 GB) between consecutive steps",
                    "step_bytes": step_bytes},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": ncu_traffic("paged_decode_kernel<128,2>"),
                      "kernel": "paged_decode_kernel<128,2> + decode_merge_kernel<128,2>", "peak_source": peak_src,
                      "attn_kernel_ms": attn_ms, "kv_store_ms": store_ms},
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d,
