@@ -81,6 +81,24 @@ def prefill_bytes(b):
     return kv + 2 * int(b.q.shape[0]) * b.num_q_heads * b.head_dim * 2
 
 
+# ------------------------------------------------------------ multi-rank timing
+
+def job_throughput(total_ms, steps, units_per_step, world, device="cpu"):
+    """Whole-job throughput of `world` replicas: the timed region's length is
+    the maximum over ranks, and every rank processed `units_per_step` units per
+    step.  Returns (ms per step, units per second across the job).  With more
+    than one rank this is a collective of the initialised process group."""
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        t = torch.tensor([float(total_ms)], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / steps
+    return ms_step, world * units_per_step / (ms_step * 1e-3)
+
+
 # ------------------------------------------------------------ ncu counters
 
 def ncu_traffic(kernel):
@@ -434,13 +452,6 @@ def main():
             torch.distributed.barrier()
         torch.cuda.synchronize()
 
-    def max_over_ranks(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        return float(t.item())
-
     if args.workload != "all":
         return run_single(args, pkv, dev, peaks, peak_src)
 
@@ -451,10 +462,9 @@ def main():
     barrier()
     total_ms, attn_ms, store_ms = arm.run(args.steps, args.warmup)
     barrier()
-    total_ms = max_over_ranks(total_ms)
-    ms_step = total_ms / args.steps
     step_bytes = decode_bytes(b) + store_bytes(b)
-    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+    ms_step, per_s = job_throughput(total_ms, args.steps, step_bytes, world, dev)
+    value = per_s / 1e9
     achieved = decode_bytes(b) / (attn_ms * 1e-3) / 1e9
     extra = {}
     if not args.only_main:
@@ -491,7 +501,8 @@ def main():
 
     # ---- end to end through host buffers ----
     e2e_ms, h2d, d2h = e2e_decode(pkv, b, dev, max(50, args.steps // 10), args.warmup)
-    e2e_val = world * step_bytes / (e2e_ms * 1e-3) / 1e9
+    e2e_ms, e2e_per_s = job_throughput(e2e_ms, 1, step_bytes, world, dev)
+    e2e_val = e2e_per_s / 1e9
 
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,

@@ -125,3 +125,44 @@ def test_decode_flags_bad_context_block_and_workspace(lib):
     db = DeviceBatch(lib, b)
     db.decode(max_total_blocks=1)
     assert db.status_value() & lib.DEV_WORKSPACE
+
+
+def test_decode_step_replays_from_a_cuda_graph(lib):
+    """kv_store + paged decode (split-K and its dependent merge launch) have no
+    host synchronisation, so a decode step can be captured once and replayed;
+    a replay reads the buffers' current contents."""
+    lens = [1, 300, 1000, 2048, 513]
+    b = wl.build_batch("graph", "decode", 46, [L - 1 for L in lens], [1] * len(lens), 16, 8, 128)
+    db = DeviceBatch(lib, b, store=False)
+    mtb = b.total_blocks_used
+    ws = lib.decode_workspace(b.num_seqs, 16, 8, 128, mtb)
+    out = torch.empty((b.num_seqs, 16, 128), dtype=torch.bfloat16, device="cuda")
+
+    def step():
+        lib.kv_store(db.k, db.v, db.k_cache, db.v_cache, db.slot_mapping, db.status)
+        lib.paged_decode_attn(out, db.q, db.k_cache, db.v_cache, db.block_tables,
+                              db.context_lens, b.scale, ws, mtb, db.status)
+
+    step()
+    eager = bits(out)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(2):
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(out), eager)
+    # new queries in the same buffer: the replay follows them
+    q2 = wl.normal_bf16(np.random.default_rng(7), b.q.shape)
+    db.q.copy_(bf16(q2))
+    graph.replay()
+    assert db.status_value() == 0
+    ekc, evc = oracle_caches(b)
+    want = oracle.paged_decode_attn(q2, ekc, evc, b.block_tables, b.context_lens, b.scale)
+    assert_close(out.double().cpu().numpy(), want, "graph replay with new q")
