@@ -212,10 +212,13 @@ def clone_batch(t):
 class Arm:
     """Runs one workload's step on the GPU with rotation over cache copies."""
 
-    def __init__(self, pkv, b, dev, copies):
+    def __init__(self, pkv, b, dev, copies, fused=None):
         import torch
 
         self.pkv, self.b, self.dev = pkv, b, dev
+        # A decode step stores its tokens inside the decode launch unless asked
+        # to time the two calls separately.
+        self.fused = (b.kind == "decode") if fused is None else fused
         base = device_batch(b, dev, b.k_cache is None, b.seed)
         self.copies = [base] + [clone_batch(base) for _ in range(copies - 1)]
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -232,6 +235,8 @@ class Arm:
         torch.cuda.synchronize()
 
     def store(self, i):
+        if self.fused:
+            return
         t = self.copies[i % len(self.copies)]
         self.pkv.kv_store(t["k"], t["v"], t["k_cache"], t["v_cache"], t["slot_mapping"],
                           self.status)
@@ -240,7 +245,12 @@ class Arm:
         r = i % len(self.copies)
         t = self.copies[r]
         b = self.b
-        if b.kind == "decode":
+        if b.kind == "decode" and self.fused:
+            self.pkv.paged_decode_store_attn(self.out[r], t["q"], t["k"], t["v"],
+                                             t["slot_mapping"], t["k_cache"], t["v_cache"],
+                                             t["block_tables"], t["context_lens"], b.scale,
+                                             self.ws[r], self.mtb, self.status)
+        elif b.kind == "decode":
             self.pkv.paged_decode_attn(self.out[r], t["q"], t["k_cache"], t["v_cache"],
                                        t["block_tables"], t["context_lens"], b.scale, self.ws[r],
                                        self.mtb, self.status)
@@ -299,9 +309,9 @@ def e2e_decode(pkv, b, dev, steps, warmup):
     def step():
         for k, v in host.items():
             t[k].copy_(v, non_blocking=True)
-        pkv.kv_store(t["k"], t["v"], t["k_cache"], t["v_cache"], t["slot_mapping"], status)
-        pkv.paged_decode_attn(out, t["q"], t["k_cache"], t["v_cache"], t["block_tables"],
-                              t["context_lens"], b.scale, ws, mtb, status)
+        pkv.paged_decode_store_attn(out, t["q"], t["k"], t["v"], t["slot_mapping"], t["k_cache"],
+                                    t["v_cache"], t["block_tables"], t["context_lens"], b.scale,
+                                    ws, mtb, status)
         out_host.copy_(out, non_blocking=True)
 
     for _ in range(warmup):
@@ -393,15 +403,17 @@ MAKERS = {"decode": wl.decode, "longdecode": wl.longdecode, "prefill": wl.prefil
 def run_single(args, pkv, dev, peaks, peak_src):
     """One workload alone: `steps` timed steps of store + attention."""
     b = MAKERS[args.workload](fill_cache=False)
-    arm = Arm(pkv, b, dev, copies=args.copies or DEFAULT_COPIES[args.workload])
+    arm = Arm(pkv, b, dev, copies=args.copies or DEFAULT_COPIES[args.workload],
+              fused=False if args.separate_store else None)
     total, am, sm_ = arm.run(args.steps, args.warmup)
     rec = {"workload": args.workload, "steps": args.steps, "warmup": args.warmup,
            "copies": len(arm.copies), "ms_per_step": total / args.steps, "attn_kernel_ms": am,
-           "kv_store_ms": sm_, "peak_source": peak_src}
+           "kv_store_ms": sm_, "fused_store": arm.fused, "peak_source": peak_src}
     if b.kind == "decode":
-        ach = decode_bytes(b) / (am * 1e-3) / 1e9
+        nbytes = decode_bytes(b) + (store_bytes(b) if arm.fused else 0)
+        ach = nbytes / (am * 1e-3) / 1e9
         rec.update(metric="decode GB/s", value=ach, unit="GB/s",
-                   frac=ach / peaks["hbm_gbs"], bytes=decode_bytes(b))
+                   frac=ach / peaks["hbm_gbs"], bytes=nbytes)
     else:
         tf = prefill_flops(b) / (am * 1e-3) / 1e12
         rec.update(metric="prefill TFLOP/s", value=tf, unit="TFLOP/s",
@@ -422,6 +434,8 @@ def main():
     ap.add_argument("--workload", default="all",
                     choices=["all", "decode", "longdecode", "prefill", "prefix"],
                     help="run one workload alone (small runs for profiling)")
+    ap.add_argument("--separate-store", action="store_true",
+                    help="decode: time kv_store and decode as two calls instead of the fused call")
     ap.add_argument("--copies", type=int, default=0,
                     help="rotating cache copies (0 = the default for each workload)")
     args = ap.parse_args()
@@ -457,7 +471,7 @@ def main():
 
     # ---- headline: decode batch (4 rotating copies of the 1 GiB pool) ----
     b = wl.decode(fill_cache=False)
-    arm = Arm(pkv, b, dev, copies=args.copies or 4)
+    arm = Arm(pkv, b, dev, copies=args.copies or 4, fused=False if args.separate_store else None)
     sampler.start()
     barrier()
     total_ms, attn_ms, store_ms = arm.run(args.steps, args.warmup)
@@ -465,7 +479,9 @@ def main():
     step_bytes = decode_bytes(b) + store_bytes(b)
     ms_step, per_s = job_throughput(total_ms, args.steps, step_bytes, world, dev)
     value = per_s / 1e9
-    achieved = decode_bytes(b) / (attn_ms * 1e-3) / 1e9
+    # The fused decode launch also moves the step's new K/V rows.
+    kernel_bytes = decode_bytes(b) + (store_bytes(b) if arm.fused else 0)
+    achieved = kernel_bytes / (attn_ms * 1e-3) / 1e9
     extra = {}
     if not args.only_main:
         # ---- other workloads of the path ----
@@ -509,19 +525,24 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": "decode: 64 seqs, contexts U[128,2048], 16 q / 8 kv heads, D=128, "
-                               "block 256, 1024-block permuted pool; kv_store of 64 tokens + "
-                               "paged decode attention per step",
+                               "block 256, 1024-block permuted pool; per step the 64 new tokens' "
+                               "K/V are stored and decode attention runs (fused in one launch "
+                               "unless --separate-store)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "4 rotating cache copies (4.3 GB) between consecutive steps",
                    "step_bytes": step_bytes},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                      "traffic": ncu_traffic("paged_decode_kernel<128,2>"),
-                     "kernel": "paged_decode_kernel<128,2> + decode_merge_kernel<128,2>", "peak_source": peak_src,
+                     "kernel": ("paged_decode_kernel<128,2> (kv_store fused) + decode_merge_kernel"
+                                "<128,2>" if arm.fused else
+                                "paged_decode_kernel<128,2> + decode_merge_kernel<128,2>"),
+                     "bytes_per_launch": kernel_bytes, "peak_source": peak_src,
                      "attn_kernel_ms": attn_ms, "kv_store_ms": store_ms},
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": 3 * args.steps,  # kv_store, split-K decode, merge
+        # split-K decode (+ kv_store when not fused) and the merge, per step
+        "gpu_launches": (2 if arm.fused else 3) * args.steps,
         "clocks": clocks,
     }
     line.update(extra)

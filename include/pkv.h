@@ -137,6 +137,34 @@ pkv_status pkv_paged_decode_attn(uint16_t *out, const uint16_t *q, const uint16_
                                  size_t workspace_bytes, int32_t *dev_status, void *stream);
 
 /*
+ * paged_decode_store_attn -- kv_store of this step's tokens fused with
+ * paged_decode_attn, in the same launches as paged_decode_attn alone.
+ *
+ * A decode step stores one new token per sequence and then attends over the
+ * whole context including it (nano-vllm hub page, "core tech 2": the layer
+ * writes K/V through the slot mapping, then runs attention; CSDN essay
+ * "from nanoVLLM to vLLM", Mountain 3).  Here new_k / new_v [num_seqs, Hkv, D]
+ * (contiguous) hold, in row s, the token at position context_lens[s] - 1 of
+ * sequence s, and slot_mapping[s] is its slot (-1: attend to it but do not
+ * store it).  The result and the cache afterwards are bit-identical to
+ * pkv_kv_store followed by pkv_paged_decode_attn: the work item that holds
+ * the newest token takes that token's row from new_k / new_v and, after using
+ * it, writes it to the cache; no other work item of the call reads that slot.
+ *
+ * Arguments, workspace and errors as for paged_decode_attn and kv_store
+ * (slots out of range set PKV_DEV_BAD_SLOT and are not written).
+ */
+pkv_status pkv_paged_decode_store_attn(uint16_t *out, const uint16_t *q, const uint16_t *new_k,
+                                       const uint16_t *new_v, const int32_t *slot_mapping,
+                                       uint16_t *k_cache, uint16_t *v_cache,
+                                       const int32_t *block_tables, const int32_t *context_lens,
+                                       int num_seqs, int num_q_heads, int num_kv_heads,
+                                       int head_dim, int block_size, int max_blocks_per_seq,
+                                       int64_t num_blocks, int64_t max_total_blocks, float scale,
+                                       void *workspace, size_t workspace_bytes,
+                                       int32_t *dev_status, void *stream);
+
+/*
  * paged_decode_attn_noalloc -- paged_decode_attn without a caller workspace.
  *
  * The pages have no counterpart to this call; it exists for callers of this

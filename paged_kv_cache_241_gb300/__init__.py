@@ -42,6 +42,9 @@ SIGNATURES = {
     "pkv_decode_workspace_size": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_i64]),
     "pkv_paged_decode_attn": (_c_int, [_p, _p, _p, _p, _p, _p, _c_int, _c_int, _c_int, _c_int,
                                        _c_int, _c_int, _c_i64, _c_i64, _c_f, _p, _c_sz, _p, _p]),
+    "pkv_paged_decode_store_attn": (_c_int, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _c_int, _c_int,
+                                             _c_int, _c_int, _c_int, _c_int, _c_i64, _c_i64, _c_f,
+                                             _p, _c_sz, _p, _p]),
     "pkv_paged_decode_attn_noalloc": (_c_int, [_p, _p, _p, _p, _p, _p, _c_int, _c_int, _c_int,
                                                _c_int, _c_int, _c_int, _c_i64, _c_i64, _c_f, _p,
                                                _p]),
@@ -166,6 +169,35 @@ def paged_decode_attn(out, q, k_cache, v_cache, block_tables, context_lens, scal
         float(scale), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _ptr(dev_status), _stream(stream))
     _check(st, "pkv_paged_decode_attn")
+
+
+def paged_decode_store_attn(out, q, k, v, slot_mapping, k_cache, v_cache, block_tables,
+                            context_lens, scale, workspace, max_total_blocks, dev_status=None,
+                            stream=None) -> None:
+    """One decode step: store k/v [S, Hkv, D] (row s = the newest token of
+    sequence s) at slot_mapping [S] and attend, fused (see include/pkv.h)."""
+    import torch
+
+    lib = load()
+    for name, t, dt, nd in (("out", out, torch.bfloat16, 3), ("q", q, torch.bfloat16, 3),
+                            ("k", k, torch.bfloat16, 3), ("v", v, torch.bfloat16, 3),
+                            ("slot_mapping", slot_mapping, torch.int32, 1),
+                            ("k_cache", k_cache, torch.bfloat16, 4),
+                            ("v_cache", v_cache, torch.bfloat16, 4),
+                            ("block_tables", block_tables, torch.int32, 2),
+                            ("context_lens", context_lens, torch.int32, 1)):
+        _need(t, dt, name, nd)
+    S, Hq, D = q.shape
+    NB, BS, Hkv, _ = k_cache.shape
+    if tuple(k.shape) != (S, Hkv, D) or tuple(v.shape) != (S, Hkv, D) or \
+            slot_mapping.shape[0] != S or tuple(out.shape) != (S, Hq, D):
+        raise ValueError("paged_decode_store_attn: inconsistent shapes")
+    st = lib.pkv_paged_decode_store_attn(
+        _ptr(out), _ptr(q), _ptr(k), _ptr(v), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),
+        _ptr(block_tables), _ptr(context_lens), S, Hq, Hkv, D, BS, block_tables.shape[1], NB,
+        int(max_total_blocks), float(scale), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream))
+    _check(st, "pkv_paged_decode_store_attn")
 
 
 def paged_decode_attn_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, scale,

@@ -61,6 +61,14 @@ struct DecodeParams {
   int block_size;
   int max_blocks_per_seq;
   float qscale;  // scale * log2(e)
+  // Fused store (all null unless the call also stores this step's tokens):
+  // row s of new_k / new_v is the token at position context_lens[s] - 1 of
+  // sequence s, to be written to cache slot new_slots[s].
+  const uint16_t *new_k;
+  const uint16_t *new_v;
+  const int32_t *new_slots;
+  uint16_t *k_cache_w;
+  uint16_t *v_cache_w;
 };
 
 __device__ __forceinline__ int named_bar_or(int id, int nthreads, int pred) {
@@ -393,6 +401,21 @@ __global__ void __launch_bounds__(kThreads)
     const int nblk = prefix[s + 1] - prefix[s];
     const int h0 = j * G;
 
+    // Fused store: the item that holds the sequence's newest token takes that
+    // token's K/V row from the inputs (patched into its shared-memory tiles,
+    // so it never depends on the cache write) and stores it to the cache once
+    // its tiles are consumed.  pl = the token's index inside this block.
+    int pl = -1;
+    uint4 new_krow = make_uint4(0, 0, 0, 0), new_vrow = make_uint4(0, 0, 0, 0);
+    if (p.new_k != nullptr && b == nblk - 1 && ctx[s] == p.context_lens[s]) {
+      pl = ctx[s] - 1 - b * BS;
+      if (lane < D / 8) {
+        const int64_t row = ((int64_t)s * Hkv + j) * D + lane * 8;
+        new_krow = __ldg(reinterpret_cast<const uint4 *>(p.new_k + row));
+        new_vrow = __ldg(reinterpret_cast<const uint4 *>(p.new_v + row));
+      }
+    }
+
     // q fragment from the staged copy: dim pairs (2e, 2e+1) of chunks r + 8c,
     // in log2 units.
     float2 qf[G][CPL * 4];
@@ -423,6 +446,11 @@ __global__ void __launch_bounds__(kThreads)
       if (ok) {
         const uint16_t *tile = reinterpret_cast<const uint16_t *>(tiles + st * kTileBytes);
         const int tok0 = warp * 16 + gid * 4;
+        if (pl >= 0 && (pl >> 6) == t && warp == ((pl & 63) >> 4)) {
+          if (lane < D / 8)
+            reinterpret_cast<uint4 *>(tiles + st * kTileBytes + (pl & 63) * D * 2)[lane] = new_krow;
+          __syncwarp();
+        }
         // Packed FP32x2 FMAs: even and odd dims accumulate in the two halves.
         float2 acc2[NV];
 #pragma unroll
@@ -495,6 +523,11 @@ __global__ void __launch_bounds__(kThreads)
       if (ok) {
         const uint16_t *tile = reinterpret_cast<const uint16_t *>(tiles + st * kTileBytes);
         const int tlo = warp * 16;
+        if (pl >= 0 && (pl >> 6) == t && warp == ((pl & 63) >> 4)) {
+          if (lane < D / 8)
+            reinterpret_cast<uint4 *>(tiles + st * kTileBytes + (pl & 63) * D * 2)[lane] = new_vrow;
+          __syncwarp();
+        }
         const int thi = min(tlo + 16, valid - t * kTile);
 #pragma unroll 4
         for (int tok = tlo; tok < thi; ++tok) {
@@ -517,6 +550,19 @@ __global__ void __launch_bounds__(kThreads)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
+    }
+
+    if (pl >= 0 && warp == 0) {
+      const int64_t slot = p.new_slots[s];
+      if (slot >= 0 && slot < p.num_blocks * BS) {
+        if (lane < D / 8) {
+          const int64_t row = (slot * Hkv + j) * D + lane * 8;
+          *reinterpret_cast<uint4 *>(p.k_cache_w + row) = new_krow;
+          *reinterpret_cast<uint4 *>(p.v_cache_w + row) = new_vrow;
+        }
+      } else if (slot != -1 && lane == 0) {
+        flag_status(p.status, PKV_DEV_BAD_SLOT);
+      }
     }
 
     // Epilogue: combine the four warps, then finish or publish a partial.
@@ -718,16 +764,19 @@ extern "C" size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int n
          align256((size_t)max_total_blocks * num_q_heads * head_dim * 4);
 }
 
-extern "C" pkv_status pkv_paged_decode_attn(uint16_t *out, const uint16_t *q,
-                                            const uint16_t *k_cache, const uint16_t *v_cache,
-                                            const int32_t *block_tables,
-                                            const int32_t *context_lens, int num_seqs,
-                                            int num_q_heads, int num_kv_heads, int head_dim,
-                                            int block_size, int max_blocks_per_seq,
-                                            int64_t num_blocks, int64_t max_total_blocks,
-                                            float scale, void *workspace, size_t workspace_bytes,
-                                            int32_t *dev_status, void *stream) {
-  using namespace pkv;
+namespace pkv {
+namespace {
+
+// Shared by the plain and the fused-store decode entry points (the fused one
+// passes the new tokens' rows, their slots and writable cache pointers).
+pkv_status decode_call(uint16_t *out, const uint16_t *q, const uint16_t *k_cache,
+                       const uint16_t *v_cache, const int32_t *block_tables,
+                       const int32_t *context_lens, int num_seqs, int num_q_heads,
+                       int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                       int64_t num_blocks, int64_t max_total_blocks, float scale, void *workspace,
+                       size_t workspace_bytes, int32_t *dev_status, void *stream,
+                       const uint16_t *new_k, const uint16_t *new_v, const int32_t *new_slots,
+                       uint16_t *k_cache_w, uint16_t *v_cache_w) {
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
       block_size <= 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 || max_total_blocks < 0)
     return PKV_ERR_INVALID_ARG;
@@ -770,6 +819,11 @@ extern "C" pkv_status pkv_paged_decode_attn(uint16_t *out, const uint16_t *q,
   prm.block_size = block_size;
   prm.max_blocks_per_seq = max_blocks_per_seq;
   prm.qscale = scale * kLog2e;
+  prm.new_k = new_k;
+  prm.new_v = new_v;
+  prm.new_slots = new_slots;
+  prm.k_cache_w = k_cache_w;
+  prm.v_cache_w = v_cache_w;
 
   // K/V cache as a 4-D tensor {D, Hkv, block_size, num_blocks}; a box is one
   // kv head's 64 consecutive tokens of one block.
@@ -800,6 +854,40 @@ extern "C" pkv_status pkv_paged_decode_attn(uint16_t *out, const uint16_t *q,
   PKV_DECODE_CASE(128, 8)
 #undef PKV_DECODE_CASE
   return PKV_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" pkv_status pkv_paged_decode_attn(uint16_t *out, const uint16_t *q,
+                                            const uint16_t *k_cache, const uint16_t *v_cache,
+                                            const int32_t *block_tables,
+                                            const int32_t *context_lens, int num_seqs,
+                                            int num_q_heads, int num_kv_heads, int head_dim,
+                                            int block_size, int max_blocks_per_seq,
+                                            int64_t num_blocks, int64_t max_total_blocks,
+                                            float scale, void *workspace, size_t workspace_bytes,
+                                            int32_t *dev_status, void *stream) {
+  return pkv::decode_call(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                          num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                          num_blocks, max_total_blocks, scale, workspace, workspace_bytes,
+                          dev_status, stream, nullptr, nullptr, nullptr, nullptr, nullptr);
+}
+
+extern "C" pkv_status pkv_paged_decode_store_attn(
+    uint16_t *out, const uint16_t *q, const uint16_t *new_k, const uint16_t *new_v,
+    const int32_t *slot_mapping, uint16_t *k_cache, uint16_t *v_cache,
+    const int32_t *block_tables, const int32_t *context_lens, int num_seqs, int num_q_heads,
+    int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq, int64_t num_blocks,
+    int64_t max_total_blocks, float scale, void *workspace, size_t workspace_bytes,
+    int32_t *dev_status, void *stream) {
+  using namespace pkv;
+  if (num_seqs > 0 && (!new_k || !new_v || !slot_mapping || !aligned16(new_k) || !aligned16(new_v)))
+    return PKV_ERR_INVALID_ARG;
+  return decode_call(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads,
+                     num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks,
+                     max_total_blocks, scale, workspace, workspace_bytes, dev_status, stream,
+                     new_k, new_v, slot_mapping, k_cache, v_cache);
 }
 
 // ---------------------------------------------------------------------------

@@ -166,3 +166,43 @@ def test_decode_step_replays_from_a_cuda_graph(lib):
     ekc, evc = oracle_caches(b)
     want = oracle.paged_decode_attn(q2, ekc, evc, b.block_tables, b.context_lens, b.scale)
     assert_close(out.double().cpu().numpy(), want, "graph replay with new q")
+
+
+@pytest.mark.parametrize("make", [wl.tiny, wl.decode])
+def test_fused_store_and_decode_match_the_two_calls_bit_for_bit(lib, make):
+    b = make()
+    two = DeviceBatch(lib, b)            # kv_store, then decode
+    ref = bits(two.decode())
+    fused = DeviceBatch(lib, b, store=False)
+    mtb = b.total_blocks_used
+    ws = lib.decode_workspace(b.num_seqs, b.num_q_heads, b.num_kv_heads, b.head_dim, mtb)
+    out = torch.empty_like(fused.q)
+    lib.paged_decode_store_attn(out, fused.q, fused.k, fused.v, fused.slot_mapping,
+                                fused.k_cache, fused.v_cache, fused.block_tables,
+                                fused.context_lens, b.scale, ws, mtb, fused.status)
+    assert fused.status_value() == 0
+    assert np.array_equal(bits(out), ref)
+    ekc, evc = oracle_caches(b)
+    assert np.array_equal(bits(fused.k_cache), ekc) and np.array_equal(bits(fused.v_cache), evc)
+
+
+def test_fused_store_never_reads_the_new_slot_from_the_cache(lib):
+    # stale NaN everywhere past the old context, including the new token's slot
+    lens = [1, 256, 257, 700, 2049]
+    b = wl.build_batch("fnan", "decode", 47, [L - 1 for L in lens], [1] * len(lens), 8, 2, 128,
+                       stale="nan")
+    for s_, L in enumerate(lens):  # poison the slot the new token goes to
+        slot = int(b.slot_mapping[s_])
+        b.k_cache[slot // 256, slot % 256] = 0x7FC0
+        b.v_cache[slot // 256, slot % 256] = 0x7FC0
+    db = DeviceBatch(lib, b, store=False)
+    mtb = b.total_blocks_used
+    ws = lib.decode_workspace(b.num_seqs, 8, 2, 128, mtb)
+    out = torch.empty_like(db.q)
+    lib.paged_decode_store_attn(out, db.q, db.k, db.v, db.slot_mapping, db.k_cache, db.v_cache,
+                                db.block_tables, db.context_lens, b.scale, ws, mtb, db.status)
+    assert db.status_value() == 0
+    ekc, evc = oracle_caches(b)
+    want = oracle.paged_decode_attn(b.q, ekc, evc, b.block_tables, b.context_lens, b.scale)
+    assert_close(out.double().cpu().numpy(), want, "fused decode")
+    assert np.array_equal(bits(db.k_cache), ekc) and np.array_equal(bits(db.v_cache), evc)
