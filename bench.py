@@ -472,6 +472,7 @@ def main():
     # ---- headline: decode batch (4 rotating copies of the 1 GiB pool) ----
     b = wl.decode(fill_cache=False)
     arm = Arm(pkv, b, dev, copies=args.copies or 4, fused=False if args.separate_store else None)
+    fused = arm.fused
     sampler.start()
     barrier()
     total_ms, attn_ms, store_ms = arm.run(args.steps, args.warmup)
@@ -480,7 +481,7 @@ def main():
     ms_step, per_s = job_throughput(total_ms, args.steps, step_bytes, world, dev)
     value = per_s / 1e9
     # The fused decode launch also moves the step's new K/V rows.
-    kernel_bytes = decode_bytes(b) + (store_bytes(b) if arm.fused else 0)
+    kernel_bytes = decode_bytes(b) + (store_bytes(b) if fused else 0)
     achieved = kernel_bytes / (attn_ms * 1e-3) / 1e9
     extra = {}
     if not args.only_main:
@@ -535,14 +536,14 @@ def main():
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                      "traffic": ncu_traffic("paged_decode_kernel<128,2>"),
                      "kernel": ("paged_decode_kernel<128,2> (kv_store fused) + decode_merge_kernel"
-                                "<128,2>" if arm.fused else
+                                "<128,2>" if fused else
                                 "paged_decode_kernel<128,2> + decode_merge_kernel<128,2>"),
                      "bytes_per_launch": kernel_bytes, "peak_source": peak_src,
                      "attn_kernel_ms": attn_ms, "kv_store_ms": store_ms},
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         # split-K decode (+ kv_store when not fused) and the merge, per step
-        "gpu_launches": (2 if arm.fused else 3) * args.steps,
+        "gpu_launches": (2 if fused else 3) * args.steps,
         "clocks": clocks,
     }
     line.update(extra)
