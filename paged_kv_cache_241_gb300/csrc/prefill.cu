@@ -39,10 +39,10 @@ constexpr int BN = 64;   // keys per tile
 // difference; the fill rate of the rings is the limit).
 constexpr int kKStages = 4;
 constexpr int kVStages = 4;
-// Warp 0: Q/K TMA producer; warp 1: MMA issuer; then one 4-warp softmax group
-// per head; last: V TMA producer.
+// Warp 0: Q/K TMA producer; warp 1: S = QK^T MMA issuer; then one 4-warp
+// softmax group per head; then the V TMA producer and the P.V MMA issuer.
 template <int NH>
-constexpr int threads_for() { return 96 + 128 * NH; }
+constexpr int threads_for() { return 128 + 128 * NH; }
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct PrefillParams {
@@ -73,8 +73,8 @@ struct PrefillLayout {
   static constexpr int p = v + kVStages * kKVBytes;
   static constexpr int bars = p + NH * kPBytes;
   // barriers: q_full, k_full[SK], v_full[SV], k_empty[SK], v_empty[SV],
-  // s_full[NH][2], p_full[NH], o_done[NH], drain
-  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 * NH + 2 * NH + 1;
+  // s_full[NH][2], s_free[NH][2], p_full[NH], o_done[NH], drain
+  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 4 * NH + 2 * NH + 1;
   static constexpr int misc = bars + kNumBars * 8;  // tmem address, abort flag
   static constexpr int total = misc + 16;
   static constexpr int kCols = NH * D + 2 * NH * BN;  // O per head + two S buffers per head
@@ -103,7 +103,8 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
   constexpr int XR = D / 64;  // 128-byte swizzle regions across D
   constexpr uint32_t kOCol = TmemCols<D, NH>::kO;
   constexpr uint32_t kSCol = TmemCols<D, NH>::kS;
-  constexpr int kVWarp = 2 + 4 * NH;  // V producer warp (after the softmax warpgroups)
+  constexpr int kVWarp = 2 + 4 * NH;   // V producer warp (after the softmax warpgroups)
+  constexpr int kPVWarp = 3 + 4 * NH;  // P.V MMA issuer
 
   // ---- which tile -------------------------------------------------------
   // Sequence-major order, each sequence's heaviest q tiles first, head groups
@@ -151,7 +152,8 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
   uint64_t *k_empty = v_full + kVStages;
   uint64_t *v_empty = k_empty + kKStages;
   uint64_t *s_full = v_empty + kVStages;  // [NH][2]
-  uint64_t *p_full = s_full + 2 * NH;
+  uint64_t *s_free = s_full + 2 * NH;     // [NH][2]: softmax has read that S buffer
+  uint64_t *p_full = s_free + 2 * NH;
   uint64_t *o_done = p_full + NH;
   uint64_t *drain = o_done + NH;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::misc);
@@ -171,12 +173,14 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
       mbar_init(&v_empty[i], 1);
     }
     for (int h = 0; h < NH; ++h) {
-      mbar_init(&s_full[2 * h], 1);
-      mbar_init(&s_full[2 * h + 1], 1);
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(&s_full[2 * h + b], 1);
+        mbar_init(&s_free[2 * h + b], 4);  // the 4 warps of the head's softmax group
+      }
       mbar_init(&p_full[h], 128);  // one softmax warpgroup per head
       mbar_init(&o_done[h], 1);
     }
-    mbar_init(drain, 1);
+    mbar_init(drain, 2);  // one commit from each MMA issuer
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -243,69 +247,71 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
         if (!mbar_wait_bounded(&full[i % nst], (i / nst) & 1, nullptr))
           flag_status(p.status, PKV_DEV_TIMEOUT);
     }
-  } else if (warp == 1) {
-    // ================= MMA issuer =================
+  } else if (warp == 1 || warp == kPVWarp) {
+    // ============ MMA issuers: warp 1 issues S = QK^T, the last warp O += PV ============
+    // Two issuing threads keep the tensor pipe fed while either one waits on
+    // a barrier (its queue of issued MMAs is short).  Shared-memory matrix
+    // descriptors are built once; an MMA only adds the operand's offset to
+    // the address field (bits 0-13, bytes / 16).
     if (lane == 0) {
-      constexpr uint32_t idesc_s = umma_idesc_bf16(BM, BN, false, false);
-      constexpr uint32_t idesc_o = umma_idesc_bf16(BM, D, false, true);
-      const uint32_t q_addr = smem_u32(sQ);
-      const uint32_t k_addr = smem_u32(sK);
-      const uint32_t v_addr = smem_u32(sV);
-      const uint32_t p_addr = smem_u32(sP);
-      bool ok = mbar_wait_bounded(q_full, 0, abort_flag);
-      tc_fence_after_sync();
-      auto issue_pv = [&](int jt, int h) {
-        const int pst = jt % kVStages;
+      bool ok = true;
+      if (warp == 1) {
+        constexpr uint32_t idesc_s = umma_idesc_bf16(BM, BN, false, false);
+        const uint64_t dq = umma_desc_sw128(smem_u32(sQ), 16, 1024);
+        const uint64_t dk = umma_desc_sw128(smem_u32(sK), 16, 1024);
+        ok = mbar_wait_bounded(q_full, 0, abort_flag);
+        // Per tile jt: S_h(jt) for every head into S buffer jt & 1 once K(jt)
+        // is in and the softmax has read S_h(jt - 2) out of that buffer.
+        for (int jt = 0; jt < n_kv && ok; ++jt) {
+          const int st = jt % kKStages;
+          ok = mbar_wait_bounded(&k_full[st], (jt / kKStages) & 1, abort_flag);
+          const uint64_t dk_st = dk + (uint64_t)((st * L::kKVBytes) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t a = umma_desc_sw128(p_addr + h * L::kPBytes + kk * 32, 16, 1024);
-          const uint64_t b =
-              umma_desc_sw128(v_addr + pst * L::kKVBytes + kk * 16 * 128, BN * 128, 1024);
-          umma_bf16(tmem + kOCol + h * D, a, b, idesc_o, (jt > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(&o_done[h]);
-      };
-      // P.V of tile jt-1 for every head, in head order, once V(jt-1) and that
-      // head's P are ready; then its V slot is released.  Head order also
-      // keeps every head's last P.V behind warpgroup 0, which clears the V
-      // rows past the context before it publishes its P.
-      auto pv_step = [&](int jt) {
-        bool good = mbar_wait_bounded(&v_full[jt % kVStages], (jt / kVStages) & 1, abort_flag);
-        for (int h = 0; h < NH && good; ++h) {
-          good = mbar_wait_bounded(&p_full[h], jt & 1, abort_flag);
-          if (!good) break;
-          tc_fence_after_sync();
-          issue_pv(jt, h);
-        }
-        if (good) umma_commit(&v_empty[jt % kVStages]);
-        return good;
-      };
-      // Per tile jt: S_h(jt) for every head into S buffer jt & 1 (free: the
-      // softmax of tile jt-2 was waited for before P.V(jt-2) was issued), then
-      // P.V(jt-1).  S of the next tile is computed while this tile's softmax
-      // runs.
-      for (int jt = 0; jt < n_kv && ok; ++jt) {
-        const int st = jt % kKStages;
-        ok = mbar_wait_bounded(&k_full[st], (jt / kKStages) & 1, abort_flag);
-        if (!ok) break;
-        tc_fence_after_sync();
-        for (int h = 0; h < NH; ++h) {
+          for (int h = 0; h < NH && ok; ++h) {
+            uint64_t *sf = &s_free[2 * h + (jt & 1)];
+            if (jt >= 2) ok = mbar_wait_bounded(sf, ((jt - 2) >> 1) & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after_sync();
+            const uint32_t d = tmem + kSCol + (2 * h + (jt & 1)) * BN;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk & 3) * 32;
-            const uint64_t a =
-                umma_desc_sw128(q_addr + h * L::kQBytes + (kk / 4) * BM * 128 + off, 16, 1024);
-            const uint64_t b =
-                umma_desc_sw128(k_addr + st * L::kKVBytes + (kk / 4) * BN * 128 + off, 16, 1024);
-            umma_bf16(tmem + kSCol + (2 * h + (jt & 1)) * BN, a, b, idesc_s, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk & 3) * 32;
+              umma_bf16(d, dq + (uint64_t)((h * L::kQBytes + (kk / 4) * BM * 128 + off) >> 4),
+                        dk_st + (uint64_t)(((kk / 4) * BN * 128 + off) >> 4), idesc_s,
+                        kk > 0 ? 1u : 0u);
+            }
+            umma_commit(&s_full[2 * h + (jt & 1)]);
           }
-          umma_commit(&s_full[2 * h + (jt & 1)]);
+          if (ok) umma_commit(&k_empty[st]);
         }
-        umma_commit(&k_empty[st]);
-        if (jt > 0) ok = pv_step(jt - 1);
+      } else {
+        constexpr uint32_t idesc_o = umma_idesc_bf16(BM, D, false, true);
+        const uint64_t dp = umma_desc_sw128(smem_u32(sP), 16, 1024);
+        const uint64_t dv = umma_desc_sw128(smem_u32(sV), BN * 128, 1024);
+        // Per tile jt, in head order: O_h += P_h(jt) V(jt) once V(jt) is in
+        // and the head's P is written; then the V slot is released.  Head
+        // order also keeps every head's last P.V behind warpgroup 0, which
+        // clears the V rows past the context before it publishes its P.
+        for (int jt = 0; jt < n_kv && ok; ++jt) {
+          const int pst = jt % kVStages;
+          ok = mbar_wait_bounded(&v_full[pst], (jt / kVStages) & 1, abort_flag);
+          const uint64_t dv_st = dv + (uint64_t)((pst * L::kKVBytes) >> 4);
+#pragma unroll
+          for (int h = 0; h < NH && ok; ++h) {
+            ok = mbar_wait_bounded(&p_full[h], jt & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after_sync();
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk)
+              umma_bf16(tmem + kOCol + h * D, dp + (uint64_t)((h * L::kPBytes + kk * 32) >> 4),
+                        dv_st + (uint64_t)((kk * 16 * 128) >> 4), idesc_o,
+                        (jt > 0 || kk > 0) ? 1u : 0u);
+            umma_commit(&o_done[h]);
+          }
+          if (ok) umma_commit(&v_empty[pst]);
+        }
       }
-      if (ok) ok = pv_step(n_kv - 1);
-      // Wait for every MMA this thread issued before tensor memory is freed.
+      // Wait for the MMAs of both issuers before tensor memory is freed.
       umma_commit(drain);
       if (!mbar_wait_bounded(drain, 0, nullptr)) flag_status(p.status, PKV_DEV_TIMEOUT);
     }
@@ -331,6 +337,10 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
       float sv[BN];
       static_assert(BN == 64, "S is read with one 64-column TMEM load");
       tmem_load64(tmem + lane_base + kSCol + (2 * h + (jt & 1)) * BN, sv);
+      // S is in registers: its buffer may take S(jt + 2).
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[2 * h + (jt & 1)]);
       // Tile max of the scaled logits over this row's visible keys (4-way tree).
       const bool full_row = key0 + BN - 1 <= key_limit;
       float mt;

@@ -35,6 +35,21 @@ def test_prefill_varlen_with_prefix_small(lib, D, G):
     check_prefill(lib, b)
 
 
+def test_prefill_single_tile_prompts_d128(lib):
+    # every prompt fits one 128-row query tile, some with long cached prefixes
+    b = wl.build_batch("onetile", "prefill", 66, [0, 300, 1000, 0], [1, 77, 128, 128], 16, 8, 128)
+    check_prefill(lib, b)
+
+
+@pytest.mark.parametrize("new", [[129], [256], [257], [383, 40], [640, 1, 129]])
+def test_prefill_tile_counts(lib, new):
+    # query tile counts 2, 2, 3, (3, 1), (5, 1, 2): ragged last tiles, one- and
+    # many-tile prompts in one launch, cached prefixes of 0, 256 and 512 keys
+    cached = [256 * (i % 3) for i in range(len(new))]
+    b = wl.build_batch("tiles", "prefill", 67 + sum(new), cached, new, 8, 4, 128)
+    check_prefill(lib, b)
+
+
 def test_prefill_single_long_prompt(lib):
     b = wl.build_batch("long", "prefill", 60, [0], [1500], 4, 2, 128)
     check_prefill(lib, b)
