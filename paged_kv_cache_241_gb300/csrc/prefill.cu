@@ -33,12 +33,6 @@ namespace {
 
 constexpr int BM = 128;  // query rows per tile (MMA M)
 constexpr int BN = 64;   // keys per tile
-// Ring depths.  A K slot is held until its S MMAs finish, a V slot until its
-// P.V has run; the rings turn over independently.  8 slots fill shared memory
-// for D=128 with 2 heads (measured: the split 4/4, 3/5 or 2/6 makes no
-// difference; the fill rate of the rings is the limit).
-constexpr int kKStages = 4;
-constexpr int kVStages = 4;
 // Warp 0: Q/K TMA producer; warp 1: S = QK^T MMA issuer; then one 4-warp
 // softmax group per head; then the V TMA producer and the P.V MMA issuer.
 template <int NH>
@@ -66,14 +60,20 @@ template <int D, int NH>
 struct PrefillLayout {
   static constexpr int kQBytes = BM * D * 2;   // one head's Q tile
   static constexpr int kKVBytes = BN * D * 2;  // one K or V tile
-  static constexpr int kPBytes = BM * BN * 2;  // one head's P tile
+  // Ring depths: the K/V slots that fit next to Q in 227 KiB of shared
+  // memory (at most 12).  A K slot is held until its S MMAs finish, a V slot
+  // until its P.V has run, so V gets the larger share.
+  static constexpr int kSlots0 = (232448 - 2048 - NH * kQBytes) / kKVBytes;
+  static constexpr int kSlots = kSlots0 < 12 ? kSlots0 : 12;
+  static constexpr int kKStages = kSlots * 2 / 5;
+  static constexpr int kVStages = kSlots - kKStages;
   static constexpr int q = 0;
   static constexpr int k = q + NH * kQBytes;
   static constexpr int v = k + kKStages * kKVBytes;
-  static constexpr int p = v + kVStages * kKVBytes;
-  static constexpr int bars = p + NH * kPBytes;
+  static constexpr int bars = v + kVStages * kKVBytes;
   // barriers: q_full, k_full[SK], v_full[SV], k_empty[SK], v_empty[SV],
   // s_full[NH][2], s_free[NH][2], p_full[NH], o_done[NH], drain
+  static_assert(kKStages >= 2 && kVStages >= 2, "rings too shallow");
   static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 4 * NH + 2 * NH + 1;
   static constexpr int misc = bars + kNumBars * 8;  // tmem address, abort flag
   static constexpr int total = misc + 16;
@@ -82,7 +82,9 @@ struct PrefillLayout {
 };
 
 // Tensor-memory columns (fp32, lane = query row): O_h at kO + h*D; the two S
-// buffers of head h at kS + (2h + b)*BN, b = tile index & 1.
+// buffers of head h at kS + (2h + b)*BN, b = tile index & 1.  The softmax
+// overwrites S(jt) in place with P(jt) as bf16 pairs (its first BN/2
+// columns), the A operand of that tile's P.V.
 template <int D, int NH>
 struct TmemCols {
   static constexpr uint32_t kO = 0;
@@ -101,6 +103,8 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
                          const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
   using L = PrefillLayout<D, NH>;
   constexpr int XR = D / 64;  // 128-byte swizzle regions across D
+  constexpr int kKStages = L::kKStages;
+  constexpr int kVStages = L::kVStages;
   constexpr uint32_t kOCol = TmemCols<D, NH>::kO;
   constexpr uint32_t kSCol = TmemCols<D, NH>::kS;
   constexpr int kVWarp = 2 + 4 * NH;   // V producer warp (after the softmax warpgroups)
@@ -144,7 +148,6 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
   uint8_t *sQ = smem + L::q;
   uint8_t *sK = smem + L::k;
   uint8_t *sV = smem + L::v;
-  uint8_t *sP = smem + L::p;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::bars);
   uint64_t *q_full = bars;
   uint64_t *k_full = bars + 1;
@@ -152,7 +155,7 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
   uint64_t *k_empty = v_full + kVStages;
   uint64_t *v_empty = k_empty + kKStages;
   uint64_t *s_full = v_empty + kVStages;  // [NH][2]
-  uint64_t *s_free = s_full + 2 * NH;     // [NH][2]: softmax has read that S buffer
+  uint64_t *s_free = s_full + 2 * NH;     // [NH][2]: P.V has read P out of that buffer
   uint64_t *p_full = s_free + 2 * NH;
   uint64_t *o_done = p_full + NH;
   uint64_t *drain = o_done + NH;
@@ -175,7 +178,7 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
     for (int h = 0; h < NH; ++h) {
       for (int b = 0; b < 2; ++b) {
         mbar_init(&s_full[2 * h + b], 1);
-        mbar_init(&s_free[2 * h + b], 4);  // the 4 warps of the head's softmax group
+        mbar_init(&s_free[2 * h + b], 1);
       }
       mbar_init(&p_full[h], 128);  // one softmax warpgroup per head
       mbar_init(&o_done[h], 1);
@@ -261,7 +264,7 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
         const uint64_t dk = umma_desc_sw128(smem_u32(sK), 16, 1024);
         ok = mbar_wait_bounded(q_full, 0, abort_flag);
         // Per tile jt: S_h(jt) for every head into S buffer jt & 1 once K(jt)
-        // is in and the softmax has read S_h(jt - 2) out of that buffer.
+        // is in and P.V(jt - 2) has read P_h(jt - 2) out of that buffer.
         for (int jt = 0; jt < n_kv && ok; ++jt) {
           const int st = jt % kKStages;
           ok = mbar_wait_bounded(&k_full[st], (jt / kKStages) & 1, abort_flag);
@@ -286,12 +289,12 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
         }
       } else {
         constexpr uint32_t idesc_o = umma_idesc_bf16(BM, D, false, true);
-        const uint64_t dp = umma_desc_sw128(smem_u32(sP), 16, 1024);
         const uint64_t dv = umma_desc_sw128(smem_u32(sV), BN * 128, 1024);
-        // Per tile jt, in head order: O_h += P_h(jt) V(jt) once V(jt) is in
-        // and the head's P is written; then the V slot is released.  Head
-        // order also keeps every head's last P.V behind warpgroup 0, which
-        // clears the V rows past the context before it publishes its P.
+        // Per tile jt, in head order: O_h += P_h(jt) V(jt) (P from tensor
+        // memory) once V(jt) is in and the head's P is written; then the S
+        // buffer and the V slot are released.  Head order also keeps every
+        // head's last P.V behind warpgroup 0, which clears the V rows past
+        // the context before it publishes its P.
         for (int jt = 0; jt < n_kv && ok; ++jt) {
           const int pst = jt % kVStages;
           ok = mbar_wait_bounded(&v_full[pst], (jt / kVStages) & 1, abort_flag);
@@ -301,12 +304,14 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
             ok = mbar_wait_bounded(&p_full[h], jt & 1, abort_flag);
             if (!ok) break;
             tc_fence_after_sync();
+            const uint32_t pa = tmem + kSCol + (2 * h + (jt & 1)) * BN;
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk)
-              umma_bf16(tmem + kOCol + h * D, dp + (uint64_t)((h * L::kPBytes + kk * 32) >> 4),
-                        dv_st + (uint64_t)((kk * 16 * 128) >> 4), idesc_o,
-                        (jt > 0 || kk > 0) ? 1u : 0u);
+              umma_bf16_tmem_a(tmem + kOCol + h * D, pa + kk * 8,
+                               dv_st + (uint64_t)((kk * 16 * 128) >> 4), idesc_o,
+                               (jt > 0 || kk > 0) ? 1u : 0u);
             umma_commit(&o_done[h]);
+            umma_commit(&s_free[2 * h + (jt & 1)]);
           }
           if (ok) umma_commit(&v_empty[pst]);
         }
@@ -336,11 +341,8 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
       tc_fence_after_sync();
       float sv[BN];
       static_assert(BN == 64, "S is read with one 64-column TMEM load");
-      tmem_load64(tmem + lane_base + kSCol + (2 * h + (jt & 1)) * BN, sv);
-      // S is in registers: its buffer may take S(jt + 2).
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[2 * h + (jt & 1)]);
+      const uint32_t s_addr = tmem + lane_base + kSCol + (2 * h + (jt & 1)) * BN;
+      tmem_load64(s_addr, sv);
       // Tile max of the scaled logits over this row's visible keys (4-way tree).
       const bool full_row = key0 + BN - 1 <= key_limit;
       float mt;
@@ -408,12 +410,14 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
         }
         rs = (r0 + r1) + (r2 + r3);
       }
-      if (jt > 0) {
-        // P.V of the previous tile must be complete: O may be rescaled, P reused.
+      if (jt > 0 && __any_sync(0xffffffffu, alpha < 1.f)) {
+        // O is rescaled once P.V(jt - 1) has landed in it (P.V(jt) waits for
+        // this tile's P).  P.V(jt - 2) is complete (S(jt) waited for it), so
+        // the parity wait cannot alias.
         ok = warp_wait(&o_done[h], (jt - 1) & 1, abort_flag);
         if (!ok) break;
         tc_fence_after_sync();
-        if (__any_sync(0xffffffffu, alpha < 1.f)) {
+        {
 #pragma unroll 1
           for (int cc = 0; cc < D / 32; ++cc) {
             float ov[32];
@@ -442,25 +446,22 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
           *reinterpret_cast<uint4 *>(vt + x * BN * 128 + rr * 128 + (rem & 7) * 16) =
               make_uint4(0, 0, 0, 0);
         }
+        fence_proxy_async_smem();  // the MMA reads these rows through the async proxy
       }
-      // P (bf16) into the 128B-swizzled K-major tile: row `row`, 16-byte chunk c
-      // of keys 8c..8c+7 lands at chunk c ^ (row & 7).
-      uint8_t *prow = sP + h * L::kPBytes + row * 128;
+      // P (bf16 pairs) over the first BN/2 columns of this tile's S buffer.
+      {
+        float pw[BN / 2];
 #pragma unroll
-      for (int cidx = 0; cidx < BN / 8; ++cidx) {
-        uint4 w;
-        const float *pv = &sv[cidx * 8];
-        w.x = pack_bf16x2(pv[0], pv[1]);
-        w.y = pack_bf16x2(pv[2], pv[3]);
-        w.z = pack_bf16x2(pv[4], pv[5]);
-        w.w = pack_bf16x2(pv[6], pv[7]);
-        *reinterpret_cast<uint4 *>(prow + ((cidx ^ (row & 7)) * 16)) = w;
+        for (int i = 0; i < BN / 2; ++i) pw[i] = __uint_as_float(pack_bf16x2(sv[2 * i], sv[2 * i + 1]));
+        static_assert(BN / 2 == 32, "P is written with one 32-column TMEM store");
+        tmem_store32(s_addr, pw);
       }
-      fence_proxy_async_smem();
       tc_fence_before_sync();
       mbar_arrive(&p_full[h]);
     }
-    // Epilogue: O / l -> bf16 rows.
+    // Epilogue: O / l -> bf16 rows, once the last P.V is in O.  P.V(n_kv - 3)
+    // is complete, so waiting on n_kv - 2 then n_kv - 1 cannot alias.
+    if (ok && n_kv >= 2) ok = warp_wait(&o_done[h], (n_kv - 2) & 1, abort_flag);
     if (ok) ok = warp_wait(&o_done[h], (n_kv - 1) & 1, abort_flag);
     if (ok) {
       tc_fence_after_sync();
