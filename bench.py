@@ -231,6 +231,7 @@ class Arm:
         else:
             self.out = [torch.empty((b.q.shape[0], b.num_q_heads, b.head_dim),
                                     dtype=torch.bfloat16, device=dev) for _ in range(copies)]
+            self.pws = pkv.prefill_workspace(dev)
         self.max_q = int(b.new_lens.max())
         torch.cuda.synchronize()
 
@@ -257,7 +258,7 @@ class Arm:
         else:
             self.pkv.paged_prefill_attn(self.out[r], t["q"], t["k_cache"], t["v_cache"],
                                         t["block_tables"], t["cu_q"], t["cu_k"], self.max_q,
-                                        b.scale, self.status)
+                                        b.scale, workspace=self.pws, dev_status=self.status)
 
     def run(self, steps, warmup):
         """Time `steps` steps; returns (total ms, mean attention-kernel ms, mean store ms)."""

@@ -217,6 +217,13 @@ pkv_status pkv_paged_decode_attn_noalloc(uint16_t *out, const uint16_t *q,
  * total_q = cu_seqlens_q[num_seqs]; max_seqlen_q bounds every n (a larger n
  * sets PKV_DEV_BAD_SEQLEN and its excess rows are not written).
  *
+ * workspace: device memory of at least pkv_prefill_workspace_size() bytes,
+ * 256-byte aligned, zero-filled before its first use.  It holds the counter
+ * from which the kernel's CTAs take their work; every call leaves it zeroed
+ * again, so one zero-fill at allocation is enough.  Calls that may run at the
+ * same time on the GPU (other streams, other host threads) need workspaces
+ * of their own.  Missing, short or misaligned: PKV_ERR_WORKSPACE.
+ *
  * Supported: head_dim in {64, 128}; Hq/Hkv in {1, 2, 4, 8};
  * block_size in {64, 128, 256, 512}.
  */
@@ -226,7 +233,11 @@ pkv_status pkv_paged_prefill_attn(uint16_t *out, const uint16_t *q, const uint16
                                   int num_seqs, int64_t total_q, int max_seqlen_q,
                                   int num_q_heads, int num_kv_heads, int head_dim,
                                   int block_size, int max_blocks_per_seq, int64_t num_blocks,
-                                  float scale, int32_t *dev_status, void *stream);
+                                  float scale, void *workspace, size_t workspace_bytes,
+                                  int32_t *dev_status, void *stream);
+
+/* Bytes of device workspace pkv_paged_prefill_attn needs (any shape). */
+size_t pkv_prefill_workspace_size(void);
 
 #ifdef __cplusplus
 }

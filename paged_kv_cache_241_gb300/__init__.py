@@ -11,7 +11,7 @@ has not been built, `load()` raises.
     pkv.paged_decode_attn(out, q, k_cache, v_cache, block_tables, context_lens,
                           scale, workspace, max_total_blocks)
     pkv.paged_prefill_attn(out, q, k_cache, v_cache, block_tables, cu_q, cu_k,
-                           max_seqlen_q, scale)
+                           max_seqlen_q, scale)   # workspace: one per stream, cached
 """
 from __future__ import annotations
 
@@ -50,7 +50,8 @@ SIGNATURES = {
                                                _p]),
     "pkv_paged_prefill_attn": (_c_int, [_p, _p, _p, _p, _p, _p, _p, _c_int, _c_i64, _c_int,
                                         _c_int, _c_int, _c_int, _c_int, _c_int, _c_i64, _c_f, _p,
-                                        _p]),
+                                        _c_sz, _p, _p]),
+    "pkv_prefill_workspace_size": (_c_sz, []),
 }
 
 _lib = None
@@ -223,9 +224,32 @@ def paged_decode_attn_noalloc(out, q, k_cache, v_cache, block_tables, context_le
     _check(st, "pkv_paged_decode_attn_noalloc")
 
 
+def prefill_workspace(device="cuda"):
+    """A zero-filled prefill workspace (the work counter the kernel's CTAs
+    share; every call leaves it zeroed).  Calls that may overlap on the GPU
+    need workspaces of their own."""
+    import torch
+
+    n = int(load().pkv_prefill_workspace_size())
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+_prefill_ws = {}
+
+
+def _default_prefill_workspace(device, stream):
+    # One workspace per (device, stream): calls on one stream are serialised.
+    key = (device.index, _stream(stream))
+    ws = _prefill_ws.get(key)
+    if ws is None:
+        ws = _prefill_ws[key] = prefill_workspace(device)
+    return ws
+
+
 def paged_prefill_attn(out, q, k_cache, v_cache, block_tables, cu_seqlens_q, cu_seqlens_k,
-                       max_seqlen_q, scale, dev_status=None, stream=None) -> None:
-    """out/q [T, Hq, D] bf16 packed by cu_seqlens_q; keys from the paged cache."""
+                       max_seqlen_q, scale, workspace=None, dev_status=None, stream=None) -> None:
+    """out/q [T, Hq, D] bf16 packed by cu_seqlens_q; keys from the paged cache.
+    workspace: from prefill_workspace(); by default one cached per stream."""
     import torch
 
     lib = load()
@@ -242,8 +266,11 @@ def paged_prefill_attn(out, q, k_cache, v_cache, block_tables, cu_seqlens_q, cu_
     if Dc != D or tuple(out.shape) != (T, Hq, D) or block_tables.shape[0] != S or \
             cu_seqlens_k.shape[0] != S + 1 or tuple(v_cache.shape) != tuple(k_cache.shape):
         raise ValueError("paged_prefill_attn: inconsistent shapes")
+    if workspace is None:
+        workspace = _default_prefill_workspace(q.device, stream)
     st = lib.pkv_paged_prefill_attn(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(cu_seqlens_q),
         _ptr(cu_seqlens_k), S, T, int(max_seqlen_q), Hq, Hkv, D, BS, block_tables.shape[1], NB,
-        float(scale), _ptr(dev_status), _stream(stream))
+        float(scale), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(dev_status), _stream(stream))
     _check(st, "pkv_paged_prefill_attn")

@@ -9,20 +9,26 @@
 // reorders the computation into on-chip tiles (same essay, Mountain 3).
 //
 // Design (GB300):
-//  * One CTA per (sequence, 128-query tile, pair of query heads of one GQA
-//    group); CTAs are ordered sequence-major (heaviest tiles of a sequence
-//    first) so that concurrent CTAs reuse a sequence's K/V from L2.  The two
-//    heads share every K/V tile.
-//  * Warp 0 issues TMA: the Q tiles once, then K and V tiles of 64 keys as
-//    128B-swizzled 4-D boxes {64 dims, 1 head, 64 tokens, 1 block}, the block
-//    id coming from the block table, into a 4-stage ring.
-//  * Warp 1 issues tcgen05.mma: S_h = Q_h K^T (M=128, N=64) into tensor memory,
-//    then O_h += P_h V (M=128, N=D) with V as an MN-major operand.
-//  * Warps 2-5 (one thread per query row) read S from tensor memory, apply the
-//    causal mask offset by the cached length, run the online softmax in fp32
-//    (log2 domain), rescale O in tensor memory when the row max grows, write
-//    P as bf16 into shared memory in the MMA's swizzled layout, and finally
-//    normalise O and store bf16 rows.
+//  * Persistent: one CTA per SM takes work units (sequence, 128-query tile,
+//    pair of query heads of one GQA group) from an atomic counter in a small
+//    caller workspace, in sequence-major order (a sequence's heaviest tiles
+//    first, head groups innermost), so that concurrent units reuse a
+//    sequence's K/V from L2.  All roles run across unit boundaries: the next
+//    unit's Q/K loads and first MMAs overlap this unit's last softmax and
+//    epilogue.  The two heads of a unit share every K/V tile.
+//  * Warp 0 fetches units (passing them to the other roles through a small
+//    shared ring) and issues TMA for Q and K; the last-but-one warp issues
+//    TMA for V: 128B-swizzled 4-D boxes {64 dims, 1 head, 64 tokens, 1 block}
+//    of 64-key tiles through the block table.
+//  * Warp 1 issues S_h = Q_h K^T (tcgen05.mma, M=128, N=64, fp32 in tensor
+//    memory); the last warp issues O_h += P_h V (M=128, N=D, P from tensor
+//    memory, V MN-major).  Two issuers keep the tensor pipe fed while either
+//    waits on a barrier.
+//  * Warps 2.. (one 4-warp group per head, one thread per query row) read S,
+//    apply the causal mask offset by the cached length, run the online
+//    softmax in fp32 (log2 domain), write P as bf16 into tensor memory,
+//    rescale O when the row max grows, and finally normalise O and store
+//    bf16 rows.
 #include <math.h>
 
 #include "host_common.h"
@@ -33,11 +39,20 @@ namespace {
 
 constexpr int BM = 128;  // query rows per tile (MMA M)
 constexpr int BN = 64;   // keys per tile
-// Warp 0: Q/K TMA producer; warp 1: S = QK^T MMA issuer; then one 4-warp
-// softmax group per head; then the V TMA producer and the P.V MMA issuer.
+constexpr int kUnitSlots = 4;  // depth of the shared ring of fetched units
+// Warp 0: unit fetcher + Q/K TMA producer; warp 1: S = QK^T MMA issuer; then
+// one 4-warp softmax group per head; then the V TMA producer and the P.V MMA
+// issuer.
 template <int NH>
 constexpr int threads_for() { return 128 + 128 * NH; }
 constexpr float kLog2e = 1.4426950408889634f;
+
+// Caller workspace: the unit counter and the count of CTAs that finished
+// fetching.  Zero between launches (the last CTA of each launch resets it).
+struct PrefillWorkspace {
+  unsigned int next_unit;
+  unsigned int ctas_done;
+};
 
 struct PrefillParams {
   uint16_t *out;
@@ -45,6 +60,7 @@ struct PrefillParams {
   const int32_t *cu_q;
   const int32_t *cu_k;
   int32_t *status;
+  PrefillWorkspace *ws;
   int64_t num_blocks;
   int64_t total_q;
   int num_seqs;
@@ -52,9 +68,52 @@ struct PrefillParams {
   int num_kv_heads;
   int block_size;
   int max_blocks_per_seq;
-  int q_tiles;  // ceil(max_seqlen_q / BM)
-  float qscale; // scale * log2(e)
+  int q_tiles;       // ceil(max_seqlen_q / BM)
+  unsigned int num_units;  // num_seqs * q_tiles * head groups
+  float qscale;      // scale * log2(e)
 };
+
+// One work unit: query rows [q0, q0 + rows_valid) of sequence s, query heads
+// h_first .. h_first + NH - 1, keys [0, n_kv * BN) of the sequence.
+struct Unit {
+  int s, q_begin, len_k, c, q0, rows_valid, n_kv, h_first, kvh;
+};
+
+// Unit index -> unit (sequence-major, heaviest tile of a sequence first, head
+// groups innermost).  False when the index has no work (a tile past a short
+// prompt) or its lengths are inconsistent (then PKV_DEV_BAD_SEQLEN is set).
+template <int NH>
+__device__ bool decode_unit(unsigned int idx, const PrefillParams &p, Unit &u) {
+  const int HG = p.num_q_heads / NH;
+  const int hg = (int)(idx % (unsigned)HG);
+  idx /= (unsigned)HG;
+  const int tr = (int)(idx % (unsigned)p.q_tiles);
+  const int s = (int)(idx / (unsigned)p.q_tiles);
+  const int q_begin = p.cu_q[s];
+  const int n = p.cu_q[s + 1] - q_begin;
+  const int len_k = p.cu_k[s + 1] - p.cu_k[s];
+  const int c = len_k - n;
+  if (n <= 0) return false;
+  const int ntq = (n + BM - 1) / BM;
+  if (c < 0 || len_k > p.max_blocks_per_seq * p.block_size || ntq > p.q_tiles ||
+      (int64_t)q_begin + n > p.total_q) {
+    if (tr == 0 && hg == 0) flag_status(p.status, PKV_DEV_BAD_SEQLEN);
+    if (c < 0 || len_k > p.max_blocks_per_seq * p.block_size || (int64_t)q_begin + n > p.total_q)
+      return false;
+  }
+  const int t = ntq - 1 - tr;
+  if (t < 0) return false;
+  u.s = s;
+  u.q_begin = q_begin;
+  u.len_k = len_k;
+  u.c = c;
+  u.q0 = t * BM;
+  u.rows_valid = min(BM, n - u.q0);
+  u.n_kv = (min(len_k, c + u.q0 + u.rows_valid) + BN - 1) / BN;  // keys the tile needs
+  u.h_first = hg * NH;
+  u.kvh = u.h_first / (p.num_q_heads / p.num_kv_heads);
+  return true;
+}
 
 template <int D, int NH>
 struct PrefillLayout {
@@ -71,24 +130,28 @@ struct PrefillLayout {
   static constexpr int k = q + NH * kQBytes;
   static constexpr int v = k + kKStages * kKVBytes;
   static constexpr int bars = v + kVStages * kKVBytes;
-  // barriers: q_full, k_full[SK], v_full[SV], k_empty[SK], v_empty[SV],
-  // s_full[NH][2], s_free[NH][2], p_full[NH], o_done[NH], drain
+  // barriers: q_full, q_empty, k_full[SK], v_full[SV], k_empty[SK], v_empty[SV],
+  // s_full[NH], s_free[NH], p_full[NH][2], p_free[NH][2], o_done[NH],
+  // o_free[NH], unit_full[U], unit_empty[U], drain
   static_assert(kKStages >= 2 && kVStages >= 2, "rings too shallow");
-  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 4 * NH + 2 * NH + 1;
-  static constexpr int misc = bars + kNumBars * 8;  // tmem address, abort flag
-  static constexpr int total = misc + 16;
-  static constexpr int kCols = NH * D + 2 * NH * BN;  // O per head + two S buffers per head
+  static constexpr int kNumBars =
+      2 + 2 * kKStages + 2 * kVStages + 8 * NH + 2 * kUnitSlots + 1;
+  static constexpr int misc = bars + kNumBars * 8;  // tmem address, abort flag, unit ring
+  static constexpr int total = misc + 8 + 4 * kUnitSlots;
+  static constexpr int kCols = NH * D + 2 * NH * BN;  // per head: O, one S, two P buffers
   static constexpr int kTmemCols = kCols <= 128 ? 128 : (kCols <= 256 ? 256 : 512);
 };
 
-// Tensor-memory columns (fp32, lane = query row): O_h at kO + h*D; the two S
-// buffers of head h at kS + (2h + b)*BN, b = tile index & 1.  The softmax
-// overwrites S(jt) in place with P(jt) as bf16 pairs (its first BN/2
-// columns), the A operand of that tile's P.V.
+// Tensor-memory columns (lane = query row): O_h (fp32) at kO + h*D; S_h
+// (fp32) at kS + h*BN; the two P buffers of head h (bf16 pairs, the A
+// operand of P.V) at kP + (2h + b)*BN/2, b = tile index & 1.  S is single
+// buffered: the softmax releases it as soon as it is in registers, so the
+// next S is computed while the softmax of this tile runs.
 template <int D, int NH>
 struct TmemCols {
   static constexpr uint32_t kO = 0;
   static constexpr uint32_t kS = NH * D;
+  static constexpr uint32_t kP = NH * D + NH * BN;
 };
 
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
@@ -96,6 +159,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
   return __all_sync(0xffffffffu, ok);
 }
 
+// Barrier phases below count tiles (g) and units (iu) over the CTA's whole
+// run, so they carry across unit boundaries.
 template <int D, int NH>
 __global__ void __launch_bounds__(threads_for<NH>(), 1)
     paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -107,39 +172,9 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
   constexpr int kVStages = L::kVStages;
   constexpr uint32_t kOCol = TmemCols<D, NH>::kO;
   constexpr uint32_t kSCol = TmemCols<D, NH>::kS;
+  constexpr uint32_t kPCol = TmemCols<D, NH>::kP;
   constexpr int kVWarp = 2 + 4 * NH;   // V producer warp (after the softmax warpgroups)
   constexpr int kPVWarp = 3 + 4 * NH;  // P.V MMA issuer
-
-  // ---- which tile -------------------------------------------------------
-  // Sequence-major order, each sequence's heaviest q tiles first, head groups
-  // innermost: CTAs running together share a sequence's K/V in L2.
-  const int HG = p.num_q_heads / NH;
-  int idx = blockIdx.x;
-  const int hg = idx % HG;
-  idx /= HG;
-  const int tr = idx % p.q_tiles;  // 0 = the sequence's last (heaviest) q tile
-  const int s = idx / p.q_tiles;
-  const int q_begin = p.cu_q[s];
-  const int n = p.cu_q[s + 1] - q_begin;
-  const int len_k = p.cu_k[s + 1] - p.cu_k[s];
-  const int c = len_k - n;
-  if (n <= 0) return;
-  const int ntq = (n + BM - 1) / BM;
-  if (c < 0 || len_k > p.max_blocks_per_seq * p.block_size || ntq > p.q_tiles ||
-      (int64_t)q_begin + n > p.total_q) {
-    if (tr == 0 && hg == 0 && threadIdx.x == 0) flag_status(p.status, PKV_DEV_BAD_SEQLEN);
-    if (c < 0 || len_k > p.max_blocks_per_seq * p.block_size || (int64_t)q_begin + n > p.total_q)
-      return;
-  }
-  const int t = ntq - 1 - tr;
-  if (t < 0) return;
-  const int q0 = t * BM;
-  const int rows_valid = min(BM, n - q0);
-  const int kv_end = min(len_k, c + q0 + rows_valid);  // keys needed by this tile
-  const int n_kv = (kv_end + BN - 1) / BN;
-  const int h_first = hg * NH;
-  const int G = p.num_q_heads / p.num_kv_heads;
-  const int kvh = h_first / G;
 
   // ---- shared memory ----------------------------------------------------
   extern __shared__ uint8_t smem_raw[];
@@ -150,23 +185,30 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
   uint8_t *sV = smem + L::v;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::bars);
   uint64_t *q_full = bars;
-  uint64_t *k_full = bars + 1;
+  uint64_t *q_empty = bars + 1;             // the unit's S MMAs no longer read Q
+  uint64_t *k_full = bars + 2;
   uint64_t *v_full = k_full + kKStages;
   uint64_t *k_empty = v_full + kVStages;
   uint64_t *v_empty = k_empty + kKStages;
-  uint64_t *s_full = v_empty + kVStages;  // [NH][2]
-  uint64_t *s_free = s_full + 2 * NH;     // [NH][2]: P.V has read P out of that buffer
-  uint64_t *p_full = s_free + 2 * NH;
-  uint64_t *o_done = p_full + NH;
-  uint64_t *drain = o_done + NH;
+  uint64_t *s_full = v_empty + kVStages;    // [NH]
+  uint64_t *s_free = s_full + NH;           // [NH]: the softmax has S in registers
+  uint64_t *p_full = s_free + NH;           // [NH][2]
+  uint64_t *p_free = p_full + 2 * NH;       // [NH][2]: P.V has read that P buffer
+  uint64_t *o_done = p_free + 2 * NH;       // [NH]
+  uint64_t *o_free = o_done + NH;           // [NH]: the epilogue has read O
+  uint64_t *unit_full = o_free + NH;        // [kUnitSlots]
+  uint64_t *unit_empty = unit_full + kUnitSlots;
+  uint64_t *drain = unit_empty + kUnitSlots;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::misc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::misc + 4);
+  volatile int *unit_ring = reinterpret_cast<volatile int *>(smem + L::misc + 8);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     for (int i = 0; i < kKStages; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
@@ -176,12 +218,19 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
       mbar_init(&v_empty[i], 1);
     }
     for (int h = 0; h < NH; ++h) {
+      mbar_init(&s_full[h], 1);
+      mbar_init(&s_free[h], 4);  // the 4 warps of the head's softmax group
       for (int b = 0; b < 2; ++b) {
-        mbar_init(&s_full[2 * h + b], 1);
-        mbar_init(&s_free[2 * h + b], 1);
+        mbar_init(&p_full[2 * h + b], 128);  // one softmax warpgroup per head
+        mbar_init(&p_free[2 * h + b], 1);
       }
-      mbar_init(&p_full[h], 128);  // one softmax warpgroup per head
       mbar_init(&o_done[h], 1);
+      mbar_init(&o_free[h], 4);
+    }
+    // Unit ring readers: V producer, both MMA issuers, every softmax warp.
+    for (int i = 0; i < kUnitSlots; ++i) {
+      mbar_init(&unit_full[i], 1);
+      mbar_init(&unit_empty[i], 3 + 4 * NH);
     }
     mbar_init(drain, 2);  // one commit from each MMA issuer
     *abort_flag = 0;
@@ -196,59 +245,131 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  // Physical block and in-block offset of KV tile jt (bounds-checked).
-  auto block_of = [&](int jt, int &off) {
-    const int key0 = jt * BN;
-    const int lb = key0 / p.block_size;
-    off = key0 - lb * p.block_size;
-    int blk = p.block_tables[(int64_t)s * p.max_blocks_per_seq + lb];
-    if (blk < 0 || (int64_t)blk >= p.num_blocks) {
-      flag_status(p.status, PKV_DEV_BAD_BLOCK);
-      blk = 0;
-    }
-    return blk;
+  // The next unit from the ring (all readers see the same sequence).  False
+  // at the end of the work or when the wait gives up.  Lane 0 of the calling
+  // warp releases the slot.
+  auto next_unit = [&](int &iu, Unit &u) -> bool {
+    const int slot = iu % kUnitSlots;
+    if (!warp_wait(&unit_full[slot], (iu / kUnitSlots) & 1, abort_flag)) return false;
+    const int idx = unit_ring[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&unit_empty[slot]);
+    ++iu;
+    if (idx < 0) return false;
+    decode_unit<NH>((unsigned)idx, p, u);
+    return true;
   };
 
   if (warp == 0 || warp == kVWarp) {
-    // ============ TMA producers: warp 0 loads Q and K, the last warp V ============
+    // ============ TMA producers: warp 0 fetches units and loads Q and K, ============
+    // ============ the last-but-one warp loads V                          ============
     // The K and V rings turn over independently: a K slot is free once the
     // S MMAs that read it are done, a V slot once its P.V MMAs are done.
-    if (lane == 0) {
-      const bool is_k = (warp == 0);
-      uint64_t *full = is_k ? k_full : v_full;
-      uint64_t *empty = is_k ? k_empty : v_empty;
-      uint8_t *ring = is_k ? sK : sV;
-      const CUtensorMap *map = is_k ? &tm_k : &tm_v;
-      const int nst = is_k ? kKStages : kVStages;
+    const bool is_k = (warp == 0);
+    uint64_t *full = is_k ? k_full : v_full;
+    uint64_t *empty = is_k ? k_empty : v_empty;
+    uint8_t *ring = is_k ? sK : sV;
+    const CUtensorMap *map = is_k ? &tm_k : &tm_v;
+    const int nst = is_k ? kKStages : kVStages;
+    int iu = 0, g = 0, q_loads = 0;
+    bool ok = true;
+    if (is_k && lane == 0) {
+      tma_prefetch_map(&tm_q);
+      tma_prefetch_map(&tm_k);
+    } else if (lane == 0) {
+      tma_prefetch_map(&tm_v);
+    }
+    for (;;) {
+      Unit u;
+      bool have;
       if (is_k) {
-        tma_prefetch_map(&tm_q);
-        tma_prefetch_map(&tm_k);
-        mbar_arrive_expect_tx(q_full, NH * L::kQBytes);
-        for (int h = 0; h < NH; ++h)
-          for (int x = 0; x < XR; ++x)
-            tma_load_3d(sQ + h * L::kQBytes + x * BM * 128, &tm_q, q_full, x * 64, h_first + h,
-                        q_begin + q0);
+        // Fetch the next unit with work and publish it to the ring.  A unit
+        // without work means the rest of its sequence's units have none
+        // either (later tiles, or an empty or inconsistent sequence): move the
+        // shared counter to the next sequence instead of taking them one by one.
+        int idx = -1;
+        if (lane == 0) {
+          const unsigned int per_seq = (unsigned)(p.q_tiles * (p.num_q_heads / NH));
+          for (;;) {
+            const unsigned int i = atomicAdd(&p.ws->next_unit, 1u);
+            if (i >= p.num_units) break;
+            if (decode_unit<NH>(i, p, u)) {
+              idx = (int)i;
+              break;
+            }
+            atomicMax(&p.ws->next_unit, (i / per_seq + 1) * per_seq);
+          }
+        }
+        idx = __shfl_sync(0xffffffffu, idx, 0);
+        const int slot = iu % kUnitSlots;
+        if (iu >= kUnitSlots)
+          ok = warp_wait(&unit_empty[slot], ((iu / kUnitSlots) - 1) & 1, abort_flag);
+        if (!ok) break;
+        if (lane == 0) {
+          unit_ring[slot] = idx;
+          mbar_arrive(&unit_full[slot]);
+        }
+        ++iu;
+        have = idx >= 0;
+        if (have) decode_unit<NH>((unsigned)idx, p, u);
       } else {
-        tma_prefetch_map(&tm_v);
+        have = next_unit(iu, u);
       }
-      int issued = 0;
-      for (int jt = 0; jt < n_kv; ++jt) {
-        const int st = jt % nst;
-        if (jt >= nst && !mbar_wait_bounded(&empty[st], ((jt / nst) - 1) & 1, abort_flag))
-          break;
-        int off;
-        const int blk = block_of(jt, off);
-        mbar_arrive_expect_tx(&full[st], L::kKVBytes);
-        for (int x = 0; x < XR; ++x)
-          tma_load_4d(ring + st * L::kKVBytes + x * BN * 128, map, &full[st], x * 64, kvh, off,
-                      blk);
-        issued = jt + 1;
+      if (!have) break;
+      if (lane == 0) {
+        if (is_k) {
+          // Q of this unit once the previous unit's S MMAs are done with Q.
+          if (iu >= 2) ok = mbar_wait_bounded(q_empty, (iu - 2) & 1, abort_flag);
+          if (ok) {
+            ++q_loads;
+            mbar_arrive_expect_tx(q_full, NH * L::kQBytes);
+            for (int h = 0; h < NH; ++h)
+              for (int x = 0; x < XR; ++x)
+                tma_load_3d(sQ + h * L::kQBytes + x * BM * 128, &tm_q, q_full, x * 64,
+                            u.h_first + h, u.q_begin + u.q0);
+          }
+        }
+        for (int jt = 0; jt < u.n_kv && ok; ++jt, ++g) {
+          const int st = g % nst;
+          if (g >= nst && !mbar_wait_bounded(&empty[st], ((g / nst) - 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const int key0 = jt * BN;
+          const int lb = key0 / p.block_size;
+          const int off = key0 - lb * p.block_size;
+          int blk = p.block_tables[(int64_t)u.s * p.max_blocks_per_seq + lb];
+          if (blk < 0 || (int64_t)blk >= p.num_blocks) {
+            flag_status(p.status, PKV_DEV_BAD_BLOCK);
+            blk = 0;
+          }
+          mbar_arrive_expect_tx(&full[st], L::kKVBytes);
+          for (int x = 0; x < XR; ++x)
+            tma_load_4d(ring + st * L::kKVBytes + x * BN * 128, map, &full[st], x * 64, u.kvh,
+                        off, blk);
+        }
       }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      g = __shfl_sync(0xffffffffu, g, 0);
+      if (!ok) break;
+    }
+    if (lane == 0) {
       // Do not leave while copies into this CTA's shared memory are in flight.
-      if (is_k && !mbar_wait_bounded(q_full, 0, nullptr)) flag_status(p.status, PKV_DEV_TIMEOUT);
-      for (int i = max(0, issued - nst); i < issued; ++i)
+      if (is_k && q_loads > 0 && !mbar_wait_bounded(q_full, (q_loads - 1) & 1, nullptr))
+        flag_status(p.status, PKV_DEV_TIMEOUT);
+      for (int i = max(0, g - nst); i < g; ++i)
         if (!mbar_wait_bounded(&full[i % nst], (i / nst) & 1, nullptr))
           flag_status(p.status, PKV_DEV_TIMEOUT);
+      if (is_k) {
+        // This CTA fetches no more units; the last CTA to get here leaves the
+        // workspace zeroed for the next launch.
+        __threadfence();
+        if (atomicAdd(&p.ws->ctas_done, 1u) == gridDim.x - 1) {
+          p.ws->next_unit = 0;
+          p.ws->ctas_done = 0;
+          __threadfence();
+        }
+      }
     }
   } else if (warp == 1 || warp == kPVWarp) {
     // ============ MMA issuers: warp 1 issues S = QK^T, the last warp O += PV ============
@@ -256,66 +377,83 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
     // a barrier (its queue of issued MMAs is short).  Shared-memory matrix
     // descriptors are built once; an MMA only adds the operand's offset to
     // the address field (bits 0-13, bytes / 16).
-    if (lane == 0) {
-      bool ok = true;
-      if (warp == 1) {
-        constexpr uint32_t idesc_s = umma_idesc_bf16(BM, BN, false, false);
-        const uint64_t dq = umma_desc_sw128(smem_u32(sQ), 16, 1024);
-        const uint64_t dk = umma_desc_sw128(smem_u32(sK), 16, 1024);
-        ok = mbar_wait_bounded(q_full, 0, abort_flag);
-        // Per tile jt: S_h(jt) for every head into S buffer jt & 1 once K(jt)
-        // is in and P.V(jt - 2) has read P_h(jt - 2) out of that buffer.
-        for (int jt = 0; jt < n_kv && ok; ++jt) {
-          const int st = jt % kKStages;
-          ok = mbar_wait_bounded(&k_full[st], (jt / kKStages) & 1, abort_flag);
-          const uint64_t dk_st = dk + (uint64_t)((st * L::kKVBytes) >> 4);
+    int iu = 0, g = 0;
+    bool ok = true;
+    Unit u;
+    if (warp == 1) {
+      constexpr uint32_t idesc_s = umma_idesc_bf16(BM, BN, false, false);
+      const uint64_t dq = umma_desc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t dk = umma_desc_sw128(smem_u32(sK), 16, 1024);
+      while (ok && next_unit(iu, u)) {
+        if (lane == 0) {
+          ok = mbar_wait_bounded(q_full, (iu - 1) & 1, abort_flag);
+          // Per tile: S_h for every head once K is in and the softmax has
+          // the previous S_h in registers.
+          for (int jt = 0; jt < u.n_kv && ok; ++jt, ++g) {
+            const int st = g % kKStages;
+            ok = mbar_wait_bounded(&k_full[st], (g / kKStages) & 1, abort_flag);
+            const uint64_t dk_st = dk + (uint64_t)((st * L::kKVBytes) >> 4);
 #pragma unroll
-          for (int h = 0; h < NH && ok; ++h) {
-            uint64_t *sf = &s_free[2 * h + (jt & 1)];
-            if (jt >= 2) ok = mbar_wait_bounded(sf, ((jt - 2) >> 1) & 1, abort_flag);
-            if (!ok) break;
-            tc_fence_after_sync();
-            const uint32_t d = tmem + kSCol + (2 * h + (jt & 1)) * BN;
+            for (int h = 0; h < NH && ok; ++h) {
+              if (g >= 1) ok = mbar_wait_bounded(&s_free[h], (g - 1) & 1, abort_flag);
+              if (!ok) break;
+              tc_fence_after_sync();
+              const uint32_t d = tmem + kSCol + h * BN;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk & 3) * 32;
-              umma_bf16(d, dq + (uint64_t)((h * L::kQBytes + (kk / 4) * BM * 128 + off) >> 4),
-                        dk_st + (uint64_t)(((kk / 4) * BN * 128 + off) >> 4), idesc_s,
-                        kk > 0 ? 1u : 0u);
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (kk & 3) * 32;
+                umma_bf16(d, dq + (uint64_t)((h * L::kQBytes + (kk / 4) * BM * 128 + off) >> 4),
+                          dk_st + (uint64_t)(((kk / 4) * BN * 128 + off) >> 4), idesc_s,
+                          kk > 0 ? 1u : 0u);
+              }
+              umma_commit(&s_full[h]);
             }
-            umma_commit(&s_full[2 * h + (jt & 1)]);
+            if (ok) umma_commit(&k_empty[st]);
           }
-          if (ok) umma_commit(&k_empty[st]);
+          if (ok) umma_commit(q_empty);
         }
-      } else {
-        constexpr uint32_t idesc_o = umma_idesc_bf16(BM, D, false, true);
-        const uint64_t dv = umma_desc_sw128(smem_u32(sV), BN * 128, 1024);
-        // Per tile jt, in head order: O_h += P_h(jt) V(jt) (P from tensor
-        // memory) once V(jt) is in and the head's P is written; then the S
-        // buffer and the V slot are released.  Head order also keeps every
-        // head's last P.V behind warpgroup 0, which clears the V rows past
-        // the context before it publishes its P.
-        for (int jt = 0; jt < n_kv && ok; ++jt) {
-          const int pst = jt % kVStages;
-          ok = mbar_wait_bounded(&v_full[pst], (jt / kVStages) & 1, abort_flag);
-          const uint64_t dv_st = dv + (uint64_t)((pst * L::kKVBytes) >> 4);
-#pragma unroll
-          for (int h = 0; h < NH && ok; ++h) {
-            ok = mbar_wait_bounded(&p_full[h], jt & 1, abort_flag);
-            if (!ok) break;
-            tc_fence_after_sync();
-            const uint32_t pa = tmem + kSCol + (2 * h + (jt & 1)) * BN;
-#pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)
-              umma_bf16_tmem_a(tmem + kOCol + h * D, pa + kk * 8,
-                               dv_st + (uint64_t)((kk * 16 * 128) >> 4), idesc_o,
-                               (jt > 0 || kk > 0) ? 1u : 0u);
-            umma_commit(&o_done[h]);
-            umma_commit(&s_free[2 * h + (jt & 1)]);
-          }
-          if (ok) umma_commit(&v_empty[pst]);
-        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        g = __shfl_sync(0xffffffffu, g, 0);
       }
+    } else {
+      constexpr uint32_t idesc_o = umma_idesc_bf16(BM, D, false, true);
+      const uint64_t dv = umma_desc_sw128(smem_u32(sV), BN * 128, 1024);
+      while (ok && next_unit(iu, u)) {
+        if (lane == 0) {
+          // Per tile, in head order: O_h += P_h V (P from tensor memory) once V
+          // is in and the head's P is written; then the P buffer and the V
+          // slot are released.  A unit's first P.V overwrites O_h, so it also
+          // waits until the previous unit's epilogue has read O_h.  Head order
+          // keeps every head's last P.V behind warpgroup 0, which clears the V
+          // rows past the context before it publishes its P.
+          for (int jt = 0; jt < u.n_kv && ok; ++jt, ++g) {
+            const int pst = g % kVStages;
+            ok = mbar_wait_bounded(&v_full[pst], (g / kVStages) & 1, abort_flag);
+            const uint64_t dv_st = dv + (uint64_t)((pst * L::kKVBytes) >> 4);
+#pragma unroll
+            for (int h = 0; h < NH && ok; ++h) {
+              ok = mbar_wait_bounded(&p_full[2 * h + (g & 1)], (g >> 1) & 1, abort_flag);
+              if (ok && jt == 0 && iu >= 2)
+                ok = mbar_wait_bounded(&o_free[h], (iu - 2) & 1, abort_flag);
+              if (!ok) break;
+              tc_fence_after_sync();
+              const uint32_t pa = tmem + kPCol + (2 * h + (g & 1)) * (BN / 2);
+#pragma unroll
+              for (int kk = 0; kk < BN / 16; ++kk)
+                umma_bf16_tmem_a(tmem + kOCol + h * D, pa + kk * 8,
+                                 dv_st + (uint64_t)((kk * 16 * 128) >> 4), idesc_o,
+                                 (jt > 0 || kk > 0) ? 1u : 0u);
+              umma_commit(&o_done[h]);
+              umma_commit(&p_free[2 * h + (g & 1)]);
+            }
+            if (ok) umma_commit(&v_empty[pst]);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        g = __shfl_sync(0xffffffffu, g, 0);
+      }
+    }
+    if (lane == 0) {
       // Wait for the MMAs of both issuers before tensor memory is freed.
       umma_commit(drain);
       if (!mbar_wait_bounded(drain, 0, nullptr)) flag_status(p.status, PKV_DEV_TIMEOUT);
@@ -326,98 +464,108 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
     const int quarter = warp & 3;   // TMEM lane quarter this warp may access
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-    const int key_limit = min(c + q0 + row, len_k - 1);  // last key this row may see
     const float qs = p.qscale;
-    // Running max in log2 units.  It is only raised (and O rescaled) when a
-    // tile's max exceeds it by more than 8, so P stays <= 2^8; l and O share
-    // the same reference, so the final O / l is unchanged.
-    float m_ref = -INFINITY;
-    float l_run = 0.f;
+    int iu = 0, g = 0;
     bool ok = true;
-    for (int jt = 0; jt < n_kv && ok; ++jt) {
-      const int key0 = jt * BN;
-      ok = warp_wait(&s_full[2 * h + (jt & 1)], (jt >> 1) & 1, abort_flag);
-      if (!ok) break;
-      tc_fence_after_sync();
-      float sv[BN];
-      static_assert(BN == 64, "S is read with one 64-column TMEM load");
-      const uint32_t s_addr = tmem + lane_base + kSCol + (2 * h + (jt & 1)) * BN;
-      tmem_load64(s_addr, sv);
-      // Tile max of the scaled logits over this row's visible keys (4-way tree).
-      const bool full_row = key0 + BN - 1 <= key_limit;
-      float mt;
-      {
-        float e0 = -INFINITY, e1 = -INFINITY, e2 = -INFINITY, e3 = -INFINITY;
-        if (qs >= 0.f) {
+    Unit u;
+    while (ok && next_unit(iu, u)) {
+      const int key_limit = min(u.c + u.q0 + row, u.len_k - 1);  // last key this row may see
+      // Running max in log2 units.  It is only raised (and O rescaled) when a
+      // tile's max exceeds it by more than 8, so P stays <= 2^8; l and O share
+      // the same reference, so the final O / l is unchanged.
+      float m_ref = -INFINITY;
+      float l_run = 0.f;
+      for (int jt = 0; jt < u.n_kv && ok; ++jt, ++g) {
+        const int key0 = jt * BN;
+        ok = warp_wait(&s_full[h], g & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after_sync();
+        float sv[BN];
+        static_assert(BN == 64, "S is read with one 64-column TMEM load");
+        tmem_load64(tmem + lane_base + kSCol + h * BN, sv);
+        // S is in registers: the S buffer may take the next S.
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_free[h]);
+        // Tile max of the scaled logits over this row's visible keys (4-way tree).
+        const bool full_row = key0 + BN - 1 <= key_limit;
+        float mt;
+        {
+          float e0 = -INFINITY, e1 = -INFINITY, e2 = -INFINITY, e3 = -INFINITY;
+          if (qs >= 0.f) {
+            if (full_row) {
+#pragma unroll
+              for (int i = 0; i < BN; i += 4) {
+                e0 = fmaxf(e0, sv[i]);
+                e1 = fmaxf(e1, sv[i + 1]);
+                e2 = fmaxf(e2, sv[i + 2]);
+                e3 = fmaxf(e3, sv[i + 3]);
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < BN; ++i)
+                if (key0 + i <= key_limit) e0 = fmaxf(e0, sv[i]);
+            }
+            mt = fmaxf(fmaxf(e0, e1), fmaxf(e2, e3)) * qs;
+          } else {
+            e0 = INFINITY;
+#pragma unroll
+            for (int i = 0; i < BN; ++i)
+              if (key0 + i <= key_limit) e0 = fminf(e0, sv[i]);
+            mt = e0 * qs;
+          }
+        }
+        // Key 0 is in the first tile and visible to every row, so the first tile
+        // sets a finite max (the -inf guard keeps a row with no visible key at
+        // alpha = 0 instead of NaN).
+        float alpha = 1.f;
+        if (jt == 0 || mt > m_ref + 8.f) {
+          const float m_new = fmaxf(m_ref, mt);
+          alpha = (m_ref == -INFINITY) ? 0.f : fast_exp2(m_ref - m_new);
+          m_ref = m_new;
+        }
+        float rs;
+        {
+          float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
           if (full_row) {
 #pragma unroll
             for (int i = 0; i < BN; i += 4) {
-              e0 = fmaxf(e0, sv[i]);
-              e1 = fmaxf(e1, sv[i + 1]);
-              e2 = fmaxf(e2, sv[i + 2]);
-              e3 = fmaxf(e3, sv[i + 3]);
+              sv[i] = fast_exp2(fmaf(sv[i], qs, -m_ref));
+              sv[i + 1] = fast_exp2(fmaf(sv[i + 1], qs, -m_ref));
+              sv[i + 2] = fast_exp2(fmaf(sv[i + 2], qs, -m_ref));
+              sv[i + 3] = fast_exp2(fmaf(sv[i + 3], qs, -m_ref));
+              r0 += sv[i];
+              r1 += sv[i + 1];
+              r2 += sv[i + 2];
+              r3 += sv[i + 3];
             }
           } else {
 #pragma unroll
-            for (int i = 0; i < BN; ++i)
-              if (key0 + i <= key_limit) e0 = fmaxf(e0, sv[i]);
-          }
-          mt = fmaxf(fmaxf(e0, e1), fmaxf(e2, e3)) * qs;
-        } else {
-          e0 = INFINITY;
+            for (int i = 0; i < BN; i += 4) {
 #pragma unroll
-          for (int i = 0; i < BN; ++i)
-            if (key0 + i <= key_limit) e0 = fminf(e0, sv[i]);
-          mt = e0 * qs;
+              for (int w = 0; w < 4; ++w)
+                sv[i + w] =
+                    (key0 + i + w <= key_limit) ? fast_exp2(fmaf(sv[i + w], qs, -m_ref)) : 0.f;
+              r0 += sv[i];
+              r1 += sv[i + 1];
+              r2 += sv[i + 2];
+              r3 += sv[i + 3];
+            }
+          }
+          rs = (r0 + r1) + (r2 + r3);
         }
-      }
-      // Key 0 is in the first tile and visible to every row, so the first tile
-      // sets a finite max (the -inf guard keeps a row with no visible key at
-      // alpha = 0 instead of NaN).
-      float alpha = 1.f;
-      if (jt == 0 || mt > m_ref + 8.f) {
-        const float m_new = fmaxf(m_ref, mt);
-        alpha = (m_ref == -INFINITY) ? 0.f : fast_exp2(m_ref - m_new);
-        m_ref = m_new;
-      }
-      float rs;
-      {
-        float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
-        if (full_row) {
-#pragma unroll
-          for (int i = 0; i < BN; i += 4) {
-            sv[i] = fast_exp2(fmaf(sv[i], qs, -m_ref));
-            sv[i + 1] = fast_exp2(fmaf(sv[i + 1], qs, -m_ref));
-            sv[i + 2] = fast_exp2(fmaf(sv[i + 2], qs, -m_ref));
-            sv[i + 3] = fast_exp2(fmaf(sv[i + 3], qs, -m_ref));
-            r0 += sv[i];
-            r1 += sv[i + 1];
-            r2 += sv[i + 2];
-            r3 += sv[i + 3];
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < BN; i += 4) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-              sv[i + u] =
-                  (key0 + i + u <= key_limit) ? fast_exp2(fmaf(sv[i + u], qs, -m_ref)) : 0.f;
-            r0 += sv[i];
-            r1 += sv[i + 1];
-            r2 += sv[i + 2];
-            r3 += sv[i + 3];
-          }
+        // P buffer g & 1 is free once the P.V two tiles back has read it.
+        if (g >= 2) {
+          ok = warp_wait(&p_free[2 * h + (g & 1)], ((g - 2) >> 1) & 1, abort_flag);
+          if (!ok) break;
         }
-        rs = (r0 + r1) + (r2 + r3);
-      }
-      if (jt > 0 && __any_sync(0xffffffffu, alpha < 1.f)) {
-        // O is rescaled once P.V(jt - 1) has landed in it (P.V(jt) waits for
-        // this tile's P).  P.V(jt - 2) is complete (S(jt) waited for it), so
-        // the parity wait cannot alias.
-        ok = warp_wait(&o_done[h], (jt - 1) & 1, abort_flag);
-        if (!ok) break;
-        tc_fence_after_sync();
-        {
+        if (jt > 0 && __any_sync(0xffffffffu, alpha < 1.f)) {
+          // O is rescaled once the previous P.V has landed in it (the next
+          // waits for this tile's P).  The P.V two tiles back is complete
+          // (waited for above), so the parity wait cannot alias.
+          ok = warp_wait(&o_done[h], (g - 1) & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after_sync();
 #pragma unroll 1
           for (int cc = 0; cc < D / 32; ++cc) {
             float ov[32];
@@ -428,50 +576,53 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
             tmem_store32(oa, ov);
           }
         }
-      }
-      l_run = l_run * alpha + rs;
-      if (h == 0 && key0 + BN > len_k) {
-        // Keys past the context may hold stale bits (even NaN); P is zero
-        // there, but 0 * NaN is not, so clear those V rows first.  (The MMA
-        // thread issues every head's last P.V after this warpgroup's arrival.)
-        ok = warp_wait(&v_full[jt % kVStages], (jt / kVStages) & 1, abort_flag);
-        if (!ok) break;
-        const int first = len_k - key0;
-        uint8_t *vt = sV + (jt % kVStages) * L::kKVBytes;
-        const int nchunks = (BN - first) * 8 * XR;  // 16-byte chunks to clear
-        for (int i = row; i < nchunks; i += 128) {
-          const int x = i / ((BN - first) * 8);
-          const int rem = i - x * (BN - first) * 8;
-          const int rr = first + rem / 8;
-          *reinterpret_cast<uint4 *>(vt + x * BN * 128 + rr * 128 + (rem & 7) * 16) =
-              make_uint4(0, 0, 0, 0);
+        l_run = l_run * alpha + rs;
+        if (h == 0 && key0 + BN > u.len_k) {
+          // Keys past the context may hold stale bits (even NaN); P is zero
+          // there, but 0 * NaN is not, so clear those V rows first.  (Every
+          // head's last P.V is issued after this warpgroup's arrival.)
+          ok = warp_wait(&v_full[g % kVStages], (g / kVStages) & 1, abort_flag);
+          if (!ok) break;
+          const int first = u.len_k - key0;
+          uint8_t *vt = sV + (g % kVStages) * L::kKVBytes;
+          const int nchunks = (BN - first) * 8 * XR;  // 16-byte chunks to clear
+          for (int i = row; i < nchunks; i += 128) {
+            const int x = i / ((BN - first) * 8);
+            const int rem = i - x * (BN - first) * 8;
+            const int rr = first + rem / 8;
+            *reinterpret_cast<uint4 *>(vt + x * BN * 128 + rr * 128 + (rem & 7) * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();  // the MMA reads these rows through the async proxy
         }
-        fence_proxy_async_smem();  // the MMA reads these rows through the async proxy
-      }
-      // P (bf16 pairs) over the first BN/2 columns of this tile's S buffer.
-      {
-        float pw[BN / 2];
+        // P (bf16 pairs) into P buffer g & 1.
+        {
+          float pw[BN / 2];
 #pragma unroll
-        for (int i = 0; i < BN / 2; ++i) pw[i] = __uint_as_float(pack_bf16x2(sv[2 * i], sv[2 * i + 1]));
-        static_assert(BN / 2 == 32, "P is written with one 32-column TMEM store");
-        tmem_store32(s_addr, pw);
+          for (int i = 0; i < BN / 2; ++i)
+            pw[i] = __uint_as_float(pack_bf16x2(sv[2 * i], sv[2 * i + 1]));
+          static_assert(BN / 2 == 32, "P is written with one 32-column TMEM store");
+          tmem_store32(tmem + lane_base + kPCol + (2 * h + (g & 1)) * (BN / 2), pw);
+        }
+        tc_fence_before_sync();
+        mbar_arrive(&p_full[2 * h + (g & 1)]);
       }
-      tc_fence_before_sync();
-      mbar_arrive(&p_full[h]);
-    }
-    // Epilogue: O / l -> bf16 rows, once the last P.V is in O.  P.V(n_kv - 3)
-    // is complete, so waiting on n_kv - 2 then n_kv - 1 cannot alias.
-    if (ok && n_kv >= 2) ok = warp_wait(&o_done[h], (n_kv - 2) & 1, abort_flag);
-    if (ok) ok = warp_wait(&o_done[h], (n_kv - 1) & 1, abort_flag);
-    if (ok) {
+      if (!ok) break;
+      // Epilogue: O / l -> bf16 rows, once the unit's last P.V (tile g - 1) is
+      // in O.  The P.V of tile g - 3 is complete (its P buffer was waited
+      // for), so waiting on g - 2 then g - 1 cannot alias.
+      if (g >= 2) ok = warp_wait(&o_done[h], (g - 2) & 1, abort_flag);
+      if (ok) ok = warp_wait(&o_done[h], (g - 1) & 1, abort_flag);
+      if (!ok) break;
       tc_fence_after_sync();
       const float inv = 1.f / l_run;
-      uint16_t *dst = p.out + ((int64_t)(q_begin + q0 + row) * p.num_q_heads + h_first + h) * D;
+      uint16_t *dst =
+          p.out + ((int64_t)(u.q_begin + u.q0 + row) * p.num_q_heads + u.h_first + h) * D;
 #pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
         float ov[32];
         tmem_load32(tmem + lane_base + kOCol + h * D + cc * 32, ov);
-        if (row < rows_valid) {
+        if (row < u.rows_valid) {
 #pragma unroll
           for (int i = 0; i < 32; i += 8) {
             uint4 w;
@@ -483,6 +634,10 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
           }
         }
       }
+      // O is read: the next unit's first P.V may overwrite it.
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&o_free[h]);
     }
     tc_fence_before_sync();
   }
@@ -513,14 +668,19 @@ pkv_status launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const CU
       return PKV_ERR_CUDA;
     smem = bytes;
   }
-  const int64_t grid = (int64_t)prm.q_tiles * prm.num_seqs * (prm.num_q_heads / NH);
-  if (grid > 0x7FFFFFFFLL) return PKV_ERR_INVALID_ARG;
+  // Persistent: as many CTAs as can be resident, no more than there are units.
+  const int ctas_per_sm = 512 / L::kTmemCols;
+  int64_t grid = (int64_t)device_sm_count() * ctas_per_sm;
+  if (grid > (int64_t)prm.num_units) grid = prm.num_units;
+  if (grid < 1) grid = 1;
   paged_prefill_kernel<D, NH><<<(unsigned)grid, threads_for<NH>(), smem, stream>>>(tq, tk, tv, prm);
   return launch_status();
 }
 
 }  // namespace
 }  // namespace pkv
+
+extern "C" size_t pkv_prefill_workspace_size(void) { return 256; }
 
 extern "C" pkv_status pkv_paged_prefill_attn(uint16_t *out, const uint16_t *q,
                                              const uint16_t *k_cache, const uint16_t *v_cache,
@@ -530,7 +690,9 @@ extern "C" pkv_status pkv_paged_prefill_attn(uint16_t *out, const uint16_t *q,
                                              int64_t total_q, int max_seqlen_q, int num_q_heads,
                                              int num_kv_heads, int head_dim, int block_size,
                                              int max_blocks_per_seq, int64_t num_blocks,
-                                             float scale, int32_t *dev_status, void *stream) {
+                                             float scale, void *workspace,
+                                             size_t workspace_bytes, int32_t *dev_status,
+                                             void *stream) {
   using namespace pkv;
   if (num_seqs < 0 || total_q < 0 || max_seqlen_q < 0 || num_q_heads <= 0 ||
       num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || max_blocks_per_seq <= 0 ||
@@ -549,6 +711,14 @@ extern "C" pkv_status pkv_paged_prefill_attn(uint16_t *out, const uint16_t *q,
     return PKV_ERR_INVALID_ARG;
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
     return PKV_ERR_INVALID_ARG;
+  if (workspace == nullptr || workspace_bytes < pkv_prefill_workspace_size() ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return PKV_ERR_WORKSPACE;
+
+  const bool two_heads = (G % 2) == 0;  // a CTA serves two query heads of one group
+  const int64_t q_tiles = (max_seqlen_q + BM - 1) / BM;
+  const int64_t units = q_tiles * num_seqs * (num_q_heads / (two_heads ? 2 : 1));
+  if (units > 0x7FFFFFFFLL) return PKV_ERR_UNSUPPORTED;
 
   PrefillParams prm;
   prm.out = out;
@@ -556,6 +726,7 @@ extern "C" pkv_status pkv_paged_prefill_attn(uint16_t *out, const uint16_t *q,
   prm.cu_q = cu_seqlens_q;
   prm.cu_k = cu_seqlens_k;
   prm.status = dev_status;
+  prm.ws = static_cast<PrefillWorkspace *>(workspace);
   prm.num_blocks = num_blocks;
   prm.total_q = total_q;
   prm.num_seqs = num_seqs;
@@ -563,7 +734,8 @@ extern "C" pkv_status pkv_paged_prefill_attn(uint16_t *out, const uint16_t *q,
   prm.num_kv_heads = num_kv_heads;
   prm.block_size = block_size;
   prm.max_blocks_per_seq = max_blocks_per_seq;
-  prm.q_tiles = (max_seqlen_q + BM - 1) / BM;
+  prm.q_tiles = (int)q_tiles;
+  prm.num_units = (unsigned int)units;
   prm.qscale = scale * kLog2e;
 
   // q as {D, Hq, T}: a box is 64 dims x 1 head x 128 query rows (swizzled).
@@ -583,8 +755,8 @@ extern "C" pkv_status pkv_paged_prefill_attn(uint16_t *out, const uint16_t *q,
     return PKV_ERR_CUDA;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const bool pair = (G % 2) == 0;
-  if (head_dim == 128) return pair ? launch_prefill<128, 2>(tq, tk, tv, prm, st)
-                                   : launch_prefill<128, 1>(tq, tk, tv, prm, st);
-  return pair ? launch_prefill<64, 2>(tq, tk, tv, prm, st) : launch_prefill<64, 1>(tq, tk, tv, prm, st);
+  if (head_dim == 128) return two_heads ? launch_prefill<128, 2>(tq, tk, tv, prm, st)
+                                        : launch_prefill<128, 1>(tq, tk, tv, prm, st);
+  return two_heads ? launch_prefill<64, 2>(tq, tk, tv, prm, st)
+                   : launch_prefill<64, 1>(tq, tk, tv, prm, st);
 }

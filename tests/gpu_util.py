@@ -70,7 +70,7 @@ class DeviceBatch:
                           device=self.dev)
         self.pkv.paged_prefill_attn(out, self.q, self.k_cache, self.v_cache, self.block_tables,
                                     self.cu_q, self.cu_k, int(b.new_lens.max()), b.scale,
-                                    self.status)
+                                    dev_status=self.status)
         return out
 
     def status_value(self):

@@ -46,7 +46,7 @@ def test_status_strings(lib):
     assert lib.pkv_status_string(0) == b"PKV_OK"
     assert lib.pkv_status_string(3) == b"PKV_ERR_WORKSPACE"
     assert lib.pkv_status_string(99) == b"PKV_ERR_UNKNOWN"
-    assert lib.pkv_abi_version() == 1
+    assert lib.pkv_abi_version() == 2
 
 
 def test_workspace_size_formula(lib):
@@ -106,7 +106,8 @@ def test_decode_rejects_bad_arguments(lib):
 
 def prefill_call(lib, **kw):
     a = dict(out=NULL, q=NULL, kc=NULL, vc=NULL, bt=NULL, cq=NULL, ck=NULL, S=2, T=100, mq=64,
-             Hq=16, Hkv=8, D=128, BS=256, maxb=4, NB=16, scale=0.1, st=NULL, stream=NULL)
+             Hq=16, Hkv=8, D=128, BS=256, maxb=4, NB=16, scale=0.1, ws=NULL, wsb=0, st=NULL,
+             stream=NULL)
     a.update(kw)
     return lib.pkv_paged_prefill_attn(*a.values())
 
@@ -119,3 +120,11 @@ def test_prefill_rejects_bad_arguments(lib):
     assert prefill_call(lib, T=-1) == 1
     assert prefill_call(lib) == 1                         # null pointers
     assert prefill_call(lib, T=0) == 0                    # nothing to do
+    # workspace missing / too small / misaligned
+    p = ctypes.c_void_p(0x10000)
+    ptrs = dict(out=p, q=p, kc=p, vc=p, bt=p, cq=p, ck=p)
+    need = lib.pkv_prefill_workspace_size()
+    assert need >= 8
+    assert prefill_call(lib, **ptrs) == 3
+    assert prefill_call(lib, **ptrs, ws=p, wsb=need - 1) == 3
+    assert prefill_call(lib, **ptrs, ws=ctypes.c_void_p(0x10010), wsb=need) == 3

@@ -111,3 +111,24 @@ def test_prefill_flags_inconsistent_seqlens(lib):
     db.cu_k[2] = db.cu_k[1] + 10  # second sequence: fewer keys than queries
     db.prefill()
     assert db.status_value() & lib.DEV_BAD_SEQLEN
+
+
+def test_prefill_workspace_is_left_zeroed_and_reusable(lib):
+    # the CTAs take units from a counter in the workspace; each call must leave
+    # it zeroed so the next call (same workspace) starts from unit 0
+    b = wl.build_batch("ws", "prefill", 68, [0, 256, 0], [700, 90, 3], 8, 4, 128)
+    db = DeviceBatch(lib, b)
+    ws = lib.prefill_workspace()
+    ekc, evc = oracle_caches(b)
+    want = oracle.paged_prefill_attn(b.q, ekc, evc, b.block_tables, b.cu_seqlens_q,
+                                     b.cu_seqlens_k, b.scale)
+    for _ in range(3):
+        out = torch.full((b.q.shape[0], b.num_q_heads, b.head_dim), float("nan"),
+                         dtype=torch.bfloat16, device="cuda")
+        lib.paged_prefill_attn(out, db.q, db.k_cache, db.v_cache, db.block_tables, db.cu_q,
+                               db.cu_k, int(b.new_lens.max()), b.scale, workspace=ws,
+                               dev_status=db.status)
+        torch.cuda.synchronize()
+        assert int(ws.count_nonzero().item()) == 0
+        assert_close(out.double().cpu().numpy(), want, "prefill, reused workspace")
+    assert db.status_value() == 0
