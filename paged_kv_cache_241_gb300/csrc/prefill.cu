@@ -609,28 +609,29 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
       }
       if (!ok) break;
       // Epilogue: O / l -> bf16 rows, once the unit's last P.V (tile g - 1) is
-      // in O.  The P.V of tile g - 3 is complete (its P buffer was waited
-      // for), so waiting on g - 2 then g - 1 cannot alias.
-      if (g >= 2) ok = warp_wait(&o_done[h], (g - 2) & 1, abort_flag);
-      if (ok) ok = warp_wait(&o_done[h], (g - 1) & 1, abort_flag);
+      // in O.  Waited for through its P buffer's barrier: that buffer's
+      // earlier use (tile g - 3) was waited for and its next use is not yet
+      // published, so the parity wait cannot alias.  (o_done could: it may be
+      // a phase further on than the wait assumes.)
+      ok = warp_wait(&p_free[2 * h + ((g - 1) & 1)], ((g - 1) >> 1) & 1, abort_flag);
       if (!ok) break;
       tc_fence_after_sync();
       const float inv = 1.f / l_run;
       uint16_t *dst =
           p.out + ((int64_t)(u.q_begin + u.q0 + row) * p.num_q_heads + u.h_first + h) * D;
 #pragma unroll 1
-      for (int cc = 0; cc < D / 32; ++cc) {
-        float ov[32];
-        tmem_load32(tmem + lane_base + kOCol + h * D + cc * 32, ov);
+      for (int half = 0; half < D / 64; ++half) {
+        float ov[64];
+        tmem_load64(tmem + lane_base + kOCol + h * D + half * 64, ov);
         if (row < u.rows_valid) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 8) {
+          for (int i = 0; i < 64; i += 8) {
             uint4 w;
             w.x = pack_bf16x2(ov[i] * inv, ov[i + 1] * inv);
             w.y = pack_bf16x2(ov[i + 2] * inv, ov[i + 3] * inv);
             w.z = pack_bf16x2(ov[i + 4] * inv, ov[i + 5] * inv);
             w.w = pack_bf16x2(ov[i + 6] * inv, ov[i + 7] * inv);
-            *reinterpret_cast<uint4 *>(dst + cc * 32 + i) = w;
+            *reinterpret_cast<uint4 *>(dst + half * 64 + i) = w;
           }
         }
       }
