@@ -71,7 +71,15 @@ struct PrefillParams {
   int q_tiles;       // ceil(max_seqlen_q / BM)
   unsigned int num_units;  // num_seqs * q_tiles * head groups
   float qscale;      // scale * log2(e)
+  int out_32b;       // out is 32-byte aligned: rows are written with 256-bit stores
 };
+
+// 32-byte store of eight 32-bit words (address 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(void *ptr, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(ptr), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
 
 // One work unit: query rows [q0, q0 + rows_valid) of sequence s, query heads
 // h_first .. h_first + NH - 1, keys [0, n_kv * BN) of the sequence.
@@ -625,13 +633,16 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
         tmem_load64(tmem + lane_base + kOCol + h * D + half * 64, ov);
         if (row < u.rows_valid) {
 #pragma unroll
-          for (int i = 0; i < 64; i += 8) {
-            uint4 w;
-            w.x = pack_bf16x2(ov[i] * inv, ov[i + 1] * inv);
-            w.y = pack_bf16x2(ov[i + 2] * inv, ov[i + 3] * inv);
-            w.z = pack_bf16x2(ov[i + 4] * inv, ov[i + 5] * inv);
-            w.w = pack_bf16x2(ov[i + 6] * inv, ov[i + 7] * inv);
-            *reinterpret_cast<uint4 *>(dst + half * 64 + i) = w;
+          for (int i = 0; i < 64; i += 16) {
+            uint32_t w[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(ov[i + 2 * e] * inv, ov[i + 2 * e + 1] * inv);
+            if (p.out_32b) {
+              st_global_v8(dst + half * 64 + i, w);
+            } else {
+              *reinterpret_cast<uint4 *>(dst + half * 64 + i) = make_uint4(w[0], w[1], w[2], w[3]);
+              *reinterpret_cast<uint4 *>(dst + half * 64 + i + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+            }
           }
         }
       }
@@ -738,6 +749,7 @@ extern "C" pkv_status pkv_paged_prefill_attn(uint16_t *out, const uint16_t *q,
   prm.q_tiles = (int)q_tiles;
   prm.num_units = (unsigned int)units;
   prm.qscale = scale * kLog2e;
+  prm.out_32b = (reinterpret_cast<uintptr_t>(out) & 31u) == 0 ? 1 : 0;
 
   // q as {D, Hq, T}: a box is 64 dims x 1 head x 128 query rows (swizzled).
   const uint64_t qdims[3] = {(uint64_t)head_dim, (uint64_t)num_q_heads, (uint64_t)total_q};

@@ -132,3 +132,22 @@ def test_prefill_workspace_is_left_zeroed_and_reusable(lib):
         assert int(ws.count_nonzero().item()) == 0
         assert_close(out.double().cpu().numpy(), want, "prefill, reused workspace")
     assert db.status_value() == 0
+
+
+def test_prefill_output_only_16_byte_aligned(lib):
+    # rows are written with 32-byte stores when `out` allows it; an `out` that
+    # is 16- but not 32-byte aligned takes the 16-byte store path
+    b = wl.build_batch("align", "prefill", 69, [0, 256], [300, 45], 8, 4, 128)
+    db = DeviceBatch(lib, b)
+    T, Hq, D = b.q.shape[0], b.num_q_heads, b.head_dim
+    buf = torch.zeros(T * Hq * D + 8, dtype=torch.bfloat16, device="cuda")
+    out = buf[8:].view(T, Hq, D)
+    assert out.data_ptr() % 32 == 16
+    lib.paged_prefill_attn(out, db.q, db.k_cache, db.v_cache, db.block_tables, db.cu_q, db.cu_k,
+                           int(b.new_lens.max()), b.scale, dev_status=db.status)
+    assert db.status_value() == 0
+    ekc, evc = oracle_caches(b)
+    want = oracle.paged_prefill_attn(b.q, ekc, evc, b.block_tables, b.cu_seqlens_q,
+                                     b.cu_seqlens_k, b.scale)
+    assert_close(out.double().cpu().numpy(), want, "prefill, 16-byte aligned out")
+    assert torch.count_nonzero(buf[:8]) == 0
