@@ -271,3 +271,40 @@ def sample_rows(rng: np.random.Generator, batch: PagedBatch, per_seq: int) -> np
             pick.update(rng.integers(a, b, size=min(per_seq, b - a)).tolist())
         rows.extend(sorted(pick))
     return np.asarray(rows, dtype=np.int64)
+
+
+# ------------------------------------------------ W4A16-G128 weight inputs
+
+@dataclass
+class W4A16Weight:
+    """A quantised weight [n, k]: packed int32 words [n, k/8] (8 nibbles each)
+    and bf16 scale bits [n, k/128] (one per 128 weights)."""
+    name: str
+    packed: np.ndarray
+    scales: np.ndarray
+
+    @property
+    def shape(self):
+        return self.packed.shape[0], self.packed.shape[1] * 8
+
+
+def w4a16_weight(name: str, seed: int, n: int, k: int) -> W4A16Weight:
+    """Uniformly random words (every nibble value equally likely) and scales
+    drawn from N(0, 0.02^2) rounded to bf16, a typical magnitude for the
+    per-group scales of a 4-bit linear layer."""
+    assert k % 128 == 0
+    rng = np.random.default_rng(seed)
+    packed = rng.integers(-(1 << 31), 1 << 31, size=(n, k // 8), dtype=np.int64).astype(np.int32)
+    scales = f32_to_bf16_bits(0.02 * rng.standard_normal(size=(n, k // 128), dtype=np.float32))
+    return W4A16Weight(name, packed, scales)
+
+
+def dequant_small() -> W4A16Weight:
+    """3 rows x 384 inputs (three groups per row): parity-test size."""
+    return w4a16_weight("dequant_small", 11, 3, 384)
+
+
+def dequant() -> W4A16Weight:
+    """One 4096 x 14336 projection (58.7M weights: 29 MB packed, 117 MB out),
+    the size of an MLP up-projection of a mid-size model."""
+    return w4a16_weight("dequant", 12, 4096, 14336)
