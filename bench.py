@@ -67,6 +67,36 @@ def store_bytes(b):
     return int(b.k.shape[0]) * b.num_kv_heads * b.head_dim * 2 * 2 * 2
 
 
+def dequant_bytes(w):
+    """W4A16-G128 dequantisation reads each 4-bit weight and its share of a
+    bf16 scale once and writes one bf16."""
+    n, k = w.shape
+    return n * k // 2 + n * (k // 128) * 2 + n * k * 2
+
+
+def time_dequant(pkv, w, dev, steps, warmup, copies=4):
+    """Mean CUDA-event time (ms) of one dequantisation of `w`, rotating over
+    `copies` input/output pairs (each pair larger than a quarter of L2)."""
+    import numpy as np
+    import torch
+
+    n, k = w.shape
+    packed = [torch.from_numpy(w.packed).to(dev) for _ in range(copies)]
+    scales = torch.from_numpy(w.scales.view(np.int16)).view(torch.bfloat16).to(dev)
+    out = [torch.empty((n, k), dtype=torch.bfloat16, device=dev) for _ in range(copies)]
+    for i in range(warmup):
+        pkv.w4a16_dequant(out[i % copies], packed[i % copies], scales)
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(steps):
+        pkv.w4a16_dequant(out[i % copies], packed[i % copies], scales)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
 def prefill_flops(b):
     """4*D*Hq per unmasked (query, key) pair."""
     c = b.cached_lens.astype(np.int64)
@@ -513,6 +543,16 @@ def main():
             extra[name] = rec
             del a2
             torch.cuda.empty_cache()
+        # W4A16-G128 weight dequantisation (a 4096 x 14336 projection)
+        w = wl.dequant()
+        dq_ms = time_dequant(pkv, w, dev, max(50, args.steps // 10), args.warmup)
+        dq = dequant_bytes(w) / (dq_ms * 1e-3) / 1e9
+        extra["w4a16_dequant"] = {"kernel_ms": dq_ms, "bytes": dequant_bytes(w),
+                                  "roofline": {"bound": "hbm", "achieved": dq,
+                                               "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                               "frac": dq / peaks["hbm_gbs"],
+                                               "traffic": ncu_traffic("w4a16_dequant_kernel")}}
+        torch.cuda.empty_cache()
     clocks = sampler.stop()
     del arm
     torch.cuda.empty_cache()

@@ -239,6 +239,26 @@ pkv_status pkv_paged_prefill_attn(uint16_t *out, const uint16_t *q, const uint16
 /* Bytes of device workspace pkv_paged_prefill_attn needs (any shape). */
 size_t pkv_prefill_workspace_size(void);
 
+/*
+ * w4a16_dequant -- W4A16-G128 weight dequantisation (s1nh.org post on
+ * upgrading nano-vllm to big-vLLM, section on quantisation: every int32 of
+ * weight_packed holds eight 4-bit values; int32 -> u4 unpack -> s4
+ * reconstruct -> float x weight_scale, one scale per 128 weights).
+ *
+ *   out[n, j] = bf16( (u4(packed[n, j / 8], j % 8) - 8) * scales[n, j / 128] )
+ *
+ * where u4(w, i) = (w >> 4i) & 15 (the lowest nibble is the first value).
+ * packed [n_rows, k/8] int32, scales [n_rows, k/128] bf16, out [n_rows, k]
+ * bf16, all row-major and contiguous, device memory owned by the caller.
+ * The product is exact in fp32 and rounded once (nearest even) to bf16.
+ *
+ * k must be a multiple of 128 and group_size 128 (PKV_ERR_INVALID_ARG /
+ * PKV_ERR_UNSUPPORTED otherwise); out and packed 16-byte aligned, scales
+ * 2-byte aligned.  n_rows == 0 or k == 0: nothing to do.
+ */
+pkv_status pkv_w4a16_dequant(uint16_t *out, const int32_t *packed, const uint16_t *scales,
+                             int64_t n_rows, int64_t k, int group_size, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -52,6 +52,7 @@ SIGNATURES = {
                                         _c_int, _c_int, _c_int, _c_int, _c_int, _c_i64, _c_f, _p,
                                         _c_sz, _p, _p]),
     "pkv_prefill_workspace_size": (_c_sz, []),
+    "pkv_w4a16_dequant": (_c_int, [_p, _p, _p, _c_i64, _c_i64, _c_int, _p]),
 }
 
 _lib = None
@@ -274,3 +275,20 @@ def paged_prefill_attn(out, q, k_cache, v_cache, block_tables, cu_seqlens_q, cu_
         float(scale), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _ptr(dev_status), _stream(stream))
     _check(st, "pkv_paged_prefill_attn")
+
+
+def w4a16_dequant(out, packed, scales, group_size=128, stream=None) -> None:
+    """out [N, K] bf16 <- packed [N, K/8] int32 (eight 4-bit values per word,
+    lowest nibble first, value = nibble - 8) times scales [N, K/128] bf16."""
+    import torch
+
+    lib = load()
+    _need(out, torch.bfloat16, "out", 2)
+    _need(packed, torch.int32, "packed", 2)
+    _need(scales, torch.bfloat16, "scales", 2)
+    N, K = out.shape
+    if tuple(packed.shape) != (N, K // 8) or tuple(scales.shape) != (N, K // group_size):
+        raise ValueError("w4a16_dequant: inconsistent shapes")
+    st = lib.pkv_w4a16_dequant(_ptr(out), _ptr(packed), _ptr(scales), N, K, int(group_size),
+                               _stream(stream))
+    _check(st, "pkv_w4a16_dequant")

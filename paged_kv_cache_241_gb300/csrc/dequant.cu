@@ -1,0 +1,105 @@
+// dequant.cu -- W4A16-G128 weight dequantisation: int32-packed 4-bit -> bf16.
+//
+// A quantised weight is an int32 tensor in which each int32 packs eight 4-bit
+// values; dequantisation is int32 -> u4 unpack -> s4 reconstruct -> float x
+// weight_scale, one scale per group of 128 weights (s1nh.org post on
+// upgrading nano-vllm to big-vLLM, section on quantisation).  Layout read
+// here: nibble i of a word is bits 4i..4i+3, s4 = u4 - 8, W [N, K] with
+// packed [N, K/8], scales [N, K/128] bf16, out [N, K] bf16.
+//
+// Design (GB300): HBM-bound streaming, 16 bytes in and 64 bytes out per 32
+// weights.  A persistent grid (SMs x 8 CTAs of 256 threads) walks 32-weight
+// chunks: one 16-byte streaming load of four words, one scale, 32 products in
+// fp32 (exact: |s4| <= 8 times a bf16 needs at most 12 significant bits),
+// each rounded once to bf16, and two 32-byte (or four 16-byte) stores.
+#include "host_common.h"
+#include "pkv_common.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kCtasPerSm = 8;
+
+__device__ __forceinline__ uint4 ld_stream_u4(const void *p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ void st_v8(void *p, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
+// Eight weights of one word, as four packed bf16 pairs (lower index in the
+// low half).  The nibble u becomes float exactly through the bit pattern
+// 0x4B000000 | u (= 2^23 + u); subtracting 2^23 + 8 gives u - 8 exactly.
+__device__ __forceinline__ void dequant_word(uint32_t word, float scale, uint32_t *out4) {
+  constexpr float kBias = 8388616.0f;  // 2^23 + 8
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t u0 = (word >> (8 * i)) & 0xFu;
+    const uint32_t u1 = (word >> (8 * i + 4)) & 0xFu;
+    const float f0 = (__uint_as_float(0x4B000000u | u0) - kBias) * scale;
+    const float f1 = (__uint_as_float(0x4B000000u | u1) - kBias) * scale;
+    out4[i] = pack_bf16x2(f0, f1);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads)
+    w4a16_dequant_kernel(uint16_t *__restrict__ out, const int32_t *__restrict__ packed,
+                         const uint16_t *__restrict__ scales, int64_t chunks,
+                         int64_t chunks_per_row, int64_t groups_per_row, int out_32b) {
+  const int64_t stride = (int64_t)gridDim.x * kThreads;
+  for (int64_t c = (int64_t)blockIdx.x * kThreads + threadIdx.x; c < chunks; c += stride) {
+    const int64_t row = c / chunks_per_row;
+    const int64_t cir = c - row * chunks_per_row;  // chunk in row: 32 weights
+    const uint4 w = ld_stream_u4(packed + c * 4);
+    const float scale =
+        __uint_as_float((uint32_t)__ldg(scales + row * groups_per_row + cir / 4) << 16);
+    uint32_t o[16];
+    dequant_word(w.x, scale, o);
+    dequant_word(w.y, scale, o + 4);
+    dequant_word(w.z, scale, o + 8);
+    dequant_word(w.w, scale, o + 12);
+    uint16_t *dst = out + c * 32;
+    if (out_32b) {
+      st_v8(dst, *reinterpret_cast<const uint32_t(*)[8]>(o));
+      st_v8(dst + 16, *reinterpret_cast<const uint32_t(*)[8]>(o + 8));
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        reinterpret_cast<uint4 *>(dst)[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+    }
+  }
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" pkv_status pkv_w4a16_dequant(uint16_t *out, const int32_t *packed,
+                                        const uint16_t *scales, int64_t n_rows, int64_t k,
+                                        int group_size, void *stream) {
+  using namespace pkv;
+  if (n_rows < 0 || k < 0) return PKV_ERR_INVALID_ARG;
+  if (group_size != 128) return PKV_ERR_UNSUPPORTED;
+  if (k % 128 != 0) return PKV_ERR_INVALID_ARG;
+  if (n_rows == 0 || k == 0) return PKV_OK;
+  if (!out || !packed || !scales) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(packed) || (reinterpret_cast<uintptr_t>(scales) & 1u) != 0)
+    return PKV_ERR_INVALID_ARG;
+  const int64_t chunks_per_row = k / 32;
+  if (n_rows > INT64_MAX / chunks_per_row) return PKV_ERR_INVALID_ARG;
+  const int64_t chunks = n_rows * chunks_per_row;
+  int64_t grid = (int64_t)device_sm_count() * kCtasPerSm;
+  const int64_t need = (chunks + kThreads - 1) / kThreads;
+  if (grid > need) grid = need;
+  const int out_32b = (reinterpret_cast<uintptr_t>(out) & 31u) == 0 ? 1 : 0;
+  w4a16_dequant_kernel<<<(unsigned)grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      out, packed, scales, chunks, chunks_per_row, k / 128, out_32b);
+  return launch_status();
+}

@@ -128,3 +128,14 @@ def test_prefill_rejects_bad_arguments(lib):
     assert prefill_call(lib, **ptrs) == 3
     assert prefill_call(lib, **ptrs, ws=p, wsb=need - 1) == 3
     assert prefill_call(lib, **ptrs, ws=ctypes.c_void_p(0x10010), wsb=need) == 3
+
+
+def test_dequant_rejects_bad_arguments(lib):
+    f = lib.pkv_w4a16_dequant
+    p = ctypes.c_void_p(0x10000)
+    assert f(p, p, p, 4, 256, 64, NULL) == 2          # only groups of 128
+    assert f(p, p, p, 4, 200, 128, NULL) == 1         # k not a multiple of 128
+    assert f(NULL, NULL, NULL, 4, 256, 128, NULL) == 1  # null pointers
+    assert f(ctypes.c_void_p(0x10008), p, p, 4, 256, 128, NULL) == 1  # out misaligned
+    assert f(p, p, ctypes.c_void_p(0x10001), 4, 256, 128, NULL) == 1  # scales misaligned
+    assert f(NULL, NULL, NULL, 0, 256, 128, NULL) == 0  # nothing to do
