@@ -97,6 +97,37 @@ def time_dequant(pkv, w, dev, steps, warmup, copies=4):
     return e0.elapsed_time(e1) / steps
 
 
+def time_block_manager(pkv, seed=13, n_seqs=1024, block_size=256):
+    """Host cost of the block manager: admit n_seqs prompts of U[256, 4096]
+    tokens, half of them opening with one shared 1024-token prefix (a system
+    prompt), then free them all; returns µs per admission and per free, and
+    the fraction of prompt tokens found in shared blocks."""
+    import time
+
+    import numpy as np
+
+    rng = np.random.default_rng(seed)
+    system = rng.integers(0, 50000, size=1024).astype(np.int32)
+    prompts = []
+    for i in range(n_seqs):
+        t = rng.integers(0, 50000, size=int(rng.integers(256, 4097))).astype(np.int32)
+        if i % 2 == 0:
+            t[: min(1024, len(t))] = system[: min(1024, len(t))]
+        prompts.append(t)
+    blocks = sum((len(t) + block_size - 1) // block_size for t in prompts)
+    bm = pkv.BlockManager(blocks, block_size)
+    t0 = time.perf_counter()
+    cached = [bm.allocate(i, t) for i, t in enumerate(prompts)]
+    t1 = time.perf_counter()
+    for i in range(n_seqs):
+        bm.free(i)
+    t2 = time.perf_counter()
+    tokens = sum(len(t) for t in prompts)
+    return {"us_per_admit": (t1 - t0) / n_seqs * 1e6, "us_per_free": (t2 - t1) / n_seqs * 1e6,
+            "prompt_tokens_per_s": tokens / (t1 - t0), "shared_token_fraction": sum(cached) / tokens,
+            "sample": f"{n_seqs} prompts, U[256, 4096] tokens, half with a shared 1024-token prefix"}
+
+
 def prefill_flops(b):
     """4*D*Hq per unmasked (query, key) pair."""
     c = b.cached_lens.astype(np.int64)
@@ -547,6 +578,7 @@ def main():
         w = wl.dequant()
         dq_ms = time_dequant(pkv, w, dev, max(50, args.steps // 10), args.warmup)
         dq = dequant_bytes(w) / (dq_ms * 1e-3) / 1e9
+        extra["block_manager"] = time_block_manager(pkv)
         extra["w4a16_dequant"] = {"kernel_ms": dq_ms, "bytes": dequant_bytes(w),
                                   "roofline": {"bound": "hbm", "achieved": dq,
                                                "peak": peaks["hbm_gbs"], "unit": "GB/s",

@@ -62,7 +62,8 @@ typedef enum pkv_status {
   PKV_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer */
   PKV_ERR_UNSUPPORTED = 2, /* head_dim, group size or block_size not built */
   PKV_ERR_WORKSPACE = 3,   /* workspace missing or too small */
-  PKV_ERR_CUDA = 4         /* a CUDA runtime/driver call or launch failed */
+  PKV_ERR_CUDA = 4,        /* a CUDA runtime/driver call or launch failed */
+  PKV_ERR_OUT_OF_BLOCKS = 5 /* block manager: not enough free blocks (nothing changed) */
 } pkv_status;
 
 /* Bits OR-ed into *dev_status by the kernels. */
@@ -258,6 +259,57 @@ size_t pkv_prefill_workspace_size(void);
  */
 pkv_status pkv_w4a16_dequant(uint16_t *out, const int32_t *packed, const uint16_t *scales,
                              int64_t n_rows, int64_t k, int group_size, void *stream);
+
+/*
+ * Block manager -- host-side allocator of the cache's blocks (no GPU work).
+ *
+ * The cache is a pool of fixed-size blocks handed out and released by
+ * reference counting (nano-vllm hub page, "core tech 4: KV Cache block
+ * manager"); a sequence takes a new block when its length reaches a multiple
+ * of the block size plus one (CSDN essay "from nanoVLLM to vLLM", Mountain
+ * 1).  Prefix sharing: every full block gets a content key, a 64-bit FNV-1a
+ * hash chained over the key of the block before it and the block's token
+ * ids; a new sequence whose prompt begins with full blocks whose keys (and
+ * tokens) match reuses those blocks, reference count + 1, and only the rest
+ * of the prompt needs kv_store and its own prefill rows.  Freed blocks keep
+ * their content and key, and stay reusable, until they are handed out again
+ * (oldest freed first; a sequence's tail is freed before its prefix).
+ *
+ * The outputs feed the kernels directly: pkv_bm_block_table gives a row of
+ * block_tables (padded with -1), pkv_bm_slots the slot_mapping of a token
+ * range, and pkv_bm_allocate the cached length c (cu_seqlens_k - cu_seqlens_q).
+ * Not thread-safe: one manager per host thread.
+ */
+typedef struct pkv_block_manager pkv_block_manager;
+
+/* num_blocks > 0 blocks of block_size tokens; NULL on bad arguments or no memory. */
+pkv_block_manager *pkv_bm_create(int num_blocks, int block_size);
+void pkv_bm_destroy(pkv_block_manager *m);
+int pkv_bm_num_free_blocks(const pkv_block_manager *m);
+
+/* Admit sequence seq_id (not yet present) with its num_tokens > 0 prompt
+ * tokens: reuses the cached leading full blocks, takes fresh ones for the
+ * rest (all or nothing: PKV_ERR_OUT_OF_BLOCKS leaves the manager unchanged).
+ * *num_cached_tokens = tokens whose K/V are already in reused blocks, at most
+ * num_tokens - 1 (the last prompt token is always computed). */
+pkv_status pkv_bm_allocate(pkv_block_manager *m, int64_t seq_id, const int32_t *tokens,
+                           int num_tokens, int *num_cached_tokens);
+/* Append one generated token (a fresh block when it starts a new one). */
+pkv_status pkv_bm_append(pkv_block_manager *m, int64_t seq_id, int32_t token);
+/* Release the sequence's blocks (reference count - 1 each). */
+pkv_status pkv_bm_free(pkv_block_manager *m, int64_t seq_id);
+
+/* Tokens held by the sequence, or -1 if unknown. */
+int pkv_bm_num_tokens(const pkv_block_manager *m, int64_t seq_id);
+/* Writes max_blocks entries of the sequence's block table (-1 past its
+ * blocks) when out != NULL; returns its block count, -1 if unknown. */
+int pkv_bm_block_table(const pkv_block_manager *m, int64_t seq_id, int32_t *out,
+                       int max_blocks);
+/* slots[i] = block_table[p / bs] * bs + p % bs for p = first .. first+count-1. */
+pkv_status pkv_bm_slots(const pkv_block_manager *m, int64_t seq_id, int first, int count,
+                        int32_t *slots);
+/* Reference count of a block (0 = free), -1 on a bad index. */
+int pkv_bm_ref_count(const pkv_block_manager *m, int block);
 
 #ifdef __cplusplus
 }

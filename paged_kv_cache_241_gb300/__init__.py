@@ -23,7 +23,8 @@ LIB_PATH = os.path.join(_HERE, "libpkv.so")
 
 PKV_OK = 0
 STATUS_NAMES = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED",
-                3: "PKV_ERR_WORKSPACE", 4: "PKV_ERR_CUDA"}
+                3: "PKV_ERR_WORKSPACE", 4: "PKV_ERR_CUDA", 5: "PKV_ERR_OUT_OF_BLOCKS"}
+PKV_ERR_OUT_OF_BLOCKS = 5
 DEV_BAD_SLOT = 0x1
 DEV_BAD_BLOCK = 0x2
 DEV_BAD_CONTEXT = 0x4
@@ -53,6 +54,16 @@ SIGNATURES = {
                                         _c_sz, _p, _p]),
     "pkv_prefill_workspace_size": (_c_sz, []),
     "pkv_w4a16_dequant": (_c_int, [_p, _p, _p, _c_i64, _c_i64, _c_int, _p]),
+    "pkv_bm_create": (_p, [_c_int, _c_int]),
+    "pkv_bm_destroy": (None, [_p]),
+    "pkv_bm_num_free_blocks": (_c_int, [_p]),
+    "pkv_bm_allocate": (_c_int, [_p, _c_i64, _p, _c_int, ctypes.POINTER(_c_int)]),
+    "pkv_bm_append": (_c_int, [_p, _c_i64, ctypes.c_int32]),
+    "pkv_bm_free": (_c_int, [_p, _c_i64]),
+    "pkv_bm_num_tokens": (_c_int, [_p, _c_i64]),
+    "pkv_bm_block_table": (_c_int, [_p, _c_i64, _p, _c_int]),
+    "pkv_bm_slots": (_c_int, [_p, _c_i64, _c_int, _c_int, _p]),
+    "pkv_bm_ref_count": (_c_int, [_p, _c_int]),
 }
 
 _lib = None
@@ -292,3 +303,72 @@ def w4a16_dequant(out, packed, scales, group_size=128, stream=None) -> None:
     st = lib.pkv_w4a16_dequant(_ptr(out), _ptr(packed), _ptr(scales), N, K, int(group_size),
                                _stream(stream))
     _check(st, "pkv_w4a16_dequant")
+
+
+class BlockManager:
+    """Host allocator of the cache's blocks with reference counts and
+    hash-chained prefix sharing (the library's pkv_bm_* calls; no GPU work).
+
+        bm = BlockManager(num_blocks, block_size=256)
+        cached = bm.allocate(seq_id, prompt_tokens)   # leading tokens already in reused blocks
+        slots = bm.slots(seq_id, cached, len(prompt_tokens) - cached)
+        row = bm.block_table(seq_id, max_blocks)
+        bm.append(seq_id, token); bm.free(seq_id)
+    """
+
+    def __init__(self, num_blocks: int, block_size: int = 256):
+        self._lib = load()
+        self._h = self._lib.pkv_bm_create(int(num_blocks), int(block_size))
+        if not self._h:
+            raise ValueError("BlockManager: bad sizes or out of host memory")
+        self.num_blocks, self.block_size = int(num_blocks), int(block_size)
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self._lib.pkv_bm_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        self.close()
+
+    @property
+    def num_free_blocks(self) -> int:
+        return int(self._lib.pkv_bm_num_free_blocks(self._h))
+
+    def allocate(self, seq_id: int, tokens) -> int:
+        import numpy as np
+
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        cached = ctypes.c_int(0)
+        _check(self._lib.pkv_bm_allocate(self._h, int(seq_id), t.ctypes.data, int(t.size),
+                                         ctypes.byref(cached)), "pkv_bm_allocate")
+        return int(cached.value)
+
+    def append(self, seq_id: int, token: int) -> None:
+        _check(self._lib.pkv_bm_append(self._h, int(seq_id), int(token)), "pkv_bm_append")
+
+    def free(self, seq_id: int) -> None:
+        _check(self._lib.pkv_bm_free(self._h, int(seq_id)), "pkv_bm_free")
+
+    def num_tokens(self, seq_id: int) -> int:
+        return int(self._lib.pkv_bm_num_tokens(self._h, int(seq_id)))
+
+    def block_table(self, seq_id: int, max_blocks: int):
+        import numpy as np
+
+        out = np.empty(int(max_blocks), dtype=np.int32)
+        n = self._lib.pkv_bm_block_table(self._h, int(seq_id), out.ctypes.data, int(max_blocks))
+        if n < 0:
+            raise KeyError(seq_id)
+        return out
+
+    def slots(self, seq_id: int, first: int, count: int):
+        import numpy as np
+
+        out = np.empty(int(count), dtype=np.int32)
+        _check(self._lib.pkv_bm_slots(self._h, int(seq_id), int(first), int(count),
+                                      out.ctypes.data), "pkv_bm_slots")
+        return out
+
+    def ref_count(self, block: int) -> int:
+        return int(self._lib.pkv_bm_ref_count(self._h, int(block)))

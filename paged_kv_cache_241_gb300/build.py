@@ -2,8 +2,9 @@
 
     python -m paged_kv_cache_241_gb300.build
 
-Compiles every csrc/*.cu in parallel with nvcc and links libpkv.so next to this
-file.  No CMake; a rebuild only recompiles sources newer than their object.
+Compiles every csrc/*.cu (and the host-only *.cpp) in parallel with nvcc and
+links libpkv.so next to this file.  No CMake; a rebuild only recompiles sources
+newer than their object.
 """
 from __future__ import annotations
 
@@ -38,7 +39,7 @@ def _headers_mtime() -> float:
 
 
 def _compile(src: str, extra: list[str]) -> str:
-    obj = os.path.join(OBJ_DIR, os.path.basename(src)[:-3] + ".o")
+    obj = os.path.join(OBJ_DIR, os.path.splitext(os.path.basename(src))[0] + ".o")
     if os.path.exists(obj) and os.path.getmtime(obj) >= max(os.path.getmtime(src), _headers_mtime()):
         return obj
     cmd = [nvcc(), *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
@@ -52,7 +53,7 @@ def _compile(src: str, extra: list[str]) -> str:
 
 def build(verbose_ptxas: bool = False) -> str:
     os.makedirs(OBJ_DIR, exist_ok=True)
-    srcs = sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
+    srcs = sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cu", ".cpp")))
     extra = ["-Xptxas", "-v"] if verbose_ptxas else []
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         objs = list(ex.map(lambda s: _compile(s, extra), srcs))

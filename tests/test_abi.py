@@ -46,7 +46,8 @@ def test_status_strings(lib):
     assert lib.pkv_status_string(0) == b"PKV_OK"
     assert lib.pkv_status_string(3) == b"PKV_ERR_WORKSPACE"
     assert lib.pkv_status_string(99) == b"PKV_ERR_UNKNOWN"
-    assert lib.pkv_abi_version() == 2
+    assert lib.pkv_abi_version() == 3
+    assert lib.pkv_status_string(5) == b"PKV_ERR_OUT_OF_BLOCKS"
 
 
 def test_workspace_size_formula(lib):

@@ -5,15 +5,16 @@
   chunked-prefill-with-decode scheduling the CSDN essay says nano-vllm lacks,
   Mountain 2);
 * shared prefix blocks: reference-counted blocks (nano-vllm hub page, "core
-  tech 4") let sequences point at the same physical blocks.
-Both run on the unchanged kernels; results are checked against the oracle."""
+  tech 4") let sequences point at the same physical blocks, here also as
+  handed out by the library's block manager (prefix caching).
+All run on the unchanged kernels; results are checked against the oracle."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
 import workloads as wl
-from gpu_util import DeviceBatch, assert_close, bits, oracle_caches
+from gpu_util import DeviceBatch, assert_close, bf16, bits, i32, oracle_caches
 
 pytestmark = pytest.mark.gpu
 
@@ -81,3 +82,81 @@ def test_prefill_over_shared_prefix_blocks(lib):
     want = oracle.paged_prefill_attn(b.q, ekc, evc, b.block_tables, b.cu_seqlens_q,
                                      b.cu_seqlens_k, b.scale)
     assert_close(out.double().cpu().numpy(), want, "prefill, shared prefix")
+
+
+def _kv_of(tokens, positions, table):
+    # K/V of a token as a fixed function of (token id, position): identical
+    # prompt prefixes give identical K/V, as a model's would
+    idx = (tokens.astype(np.int64) * 2654435761 + positions.astype(np.int64) * 40503) % len(table)
+    return table[idx]
+
+
+def test_block_manager_prefix_sharing_end_to_end(lib):
+    Hq, Hkv, D, bs, NB = 8, 4, 128, 256, 24
+    rng = np.random.default_rng(90)
+    ktab = wl.normal_bf16(rng, (4099, Hkv, D))
+    vtab = wl.normal_bf16(rng, (4099, Hkv, D))
+    a = rng.integers(0, 50000, size=700).astype(np.int32)
+    prompts = [a,
+               np.concatenate([a[:512], rng.integers(0, 50000, 288)]).astype(np.int32),
+               np.concatenate([a[:256], rng.integers(0, 50000, 44)]).astype(np.int32),
+               rng.integers(0, 50000, size=70).astype(np.int32)]
+    bm = lib.BlockManager(NB, bs)
+    cached = [bm.allocate(i, p) for i, p in enumerate(prompts)]
+    assert cached == [0, 512, 256, 0]
+    new = [len(p) - c for p, c in zip(prompts, cached)]
+    maxb = 4
+    tables = np.stack([bm.block_table(i, maxb) for i in range(4)])
+    # only the uncached tokens are stored
+    slots = np.concatenate([bm.slots(i, c, n) for i, (c, n) in enumerate(zip(cached, new))])
+    toks = np.concatenate([p[c:] for p, c in zip(prompts, cached)])
+    pos = np.concatenate([np.arange(c, len(p)) for p, c in zip(prompts, cached)])
+    k_new, v_new = _kv_of(toks, pos, ktab), _kv_of(toks, pos, vtab)
+    stale = np.full((NB, bs, Hkv, D), wl.BF16_QNAN, dtype=np.uint16)
+    q = wl.normal_bf16(rng, (sum(new), Hq, D))
+    cu_q = np.concatenate([[0], np.cumsum(new)]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum([len(p) for p in prompts])]).astype(np.int32)
+    scale = 1.0 / np.sqrt(D)
+
+    kc, vc = bf16(stale), bf16(stale)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lib.kv_store(bf16(k_new), bf16(v_new), kc, vc, i32(slots), status)
+    out = torch.empty((sum(new), Hq, D), dtype=torch.bfloat16, device="cuda")
+    lib.paged_prefill_attn(out, bf16(q), kc, vc, i32(tables), i32(cu_q), i32(cu_k), max(new),
+                           scale, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+
+    ekc, evc = oracle.kv_store(stale, stale, k_new, v_new, slots)
+    want = oracle.paged_prefill_attn(q, ekc, evc, tables, cu_q, cu_k, scale)
+    # what prefix caching must preserve: the same result as attending over
+    # each sequence's whole prompt, its K/V computed afresh
+    for s, (p, c) in enumerate(zip(prompts, cached)):
+        kf = oracle.bf16_bits_to_f64(_kv_of(p, np.arange(len(p)), ktab))
+        vf = oracle.bf16_bits_to_f64(_kv_of(p, np.arange(len(p)), vtab))
+        qf = oracle.bf16_bits_to_f64(q[cu_q[s]:cu_q[s + 1]])
+        for i in (0, new[s] - 1):
+            for h in (0, Hq - 1):
+                j = oracle.kv_head_of(h, Hq, Hkv)
+                ref = oracle.attend(qf[i, h], kf[: c + i + 1, j], vf[: c + i + 1, j], scale)
+                assert np.allclose(want[cu_q[s] + i, h], ref, rtol=1e-12, atol=1e-12)
+    assert_close(out.double().cpu().numpy(), want, "prefill over shared prefix blocks")
+
+    # one decode step per sequence on top of the shared blocks
+    nxt = rng.integers(0, 50000, size=4).astype(np.int32)
+    for i, t in enumerate(nxt):
+        bm.append(i, int(t))
+    lens = np.array([bm.num_tokens(i) for i in range(4)], dtype=np.int32)
+    tables = np.stack([bm.block_table(i, maxb) for i in range(4)])
+    slots1 = np.concatenate([bm.slots(i, int(L) - 1, 1) for i, L in enumerate(lens)])
+    k1, v1 = _kv_of(nxt, lens - 1, ktab), _kv_of(nxt, lens - 1, vtab)
+    q1 = wl.normal_bf16(rng, (4, Hq, D))
+    lib.kv_store(bf16(k1), bf16(v1), kc, vc, i32(slots1), status)
+    ws = lib.decode_workspace(4, Hq, Hkv, D, 16)
+    dec = torch.empty((4, Hq, D), dtype=torch.bfloat16, device="cuda")
+    lib.paged_decode_attn(dec, bf16(q1), kc, vc, i32(tables), i32(lens), scale, ws, 16, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ekc, evc = oracle.kv_store(ekc, evc, k1, v1, slots1)
+    want1 = oracle.paged_decode_attn(q1, ekc, evc, tables, lens, scale)
+    assert_close(dec.double().cpu().numpy(), want1, "decode over shared prefix blocks")
