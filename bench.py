@@ -459,7 +459,7 @@ def run_reference(args):
 
 DEFAULT_COPIES = {"decode": 4, "longdecode": 3, "prefill": 4, "prefix": 8}
 MAKERS = {"decode": wl.decode, "longdecode": wl.longdecode, "prefill": wl.prefill,
-          "prefix": wl.prefix}
+          "prefix": wl.prefix, "mixed": wl.mixed}
 
 
 def run_single(args, pkv, dev, peaks, peak_src):
@@ -494,7 +494,7 @@ def main():
     ap.add_argument("--only-main", action="store_true",
                     help="headline decode step only (no other workloads)")
     ap.add_argument("--workload", default="all",
-                    choices=["all", "decode", "longdecode", "prefill", "prefix"],
+                    choices=["all", "decode", "longdecode", "prefill", "prefix", "mixed"],
                     help="run one workload alone (small runs for profiling)")
     ap.add_argument("--separate-store", action="store_true",
                     help="decode: time kv_store and decode as two calls instead of the fused call")
@@ -551,7 +551,8 @@ def main():
         sub = max(20, args.steps // 10)
         for name, make, copies, steps in (("longdecode", wl.longdecode, 3, sub),
                                           ("prefill", wl.prefill, 4, sub),
-                                          ("prefix", wl.prefix, 8, sub)):
+                                          ("prefix", wl.prefix, 8, sub),
+                                          ("mixed", wl.mixed, 8, sub)):
             bb = make(fill_cache=False)
             a2 = Arm(pkv, bb, dev, copies=copies)
             tot, am, sm_ = a2.run(steps, args.warmup)

@@ -253,8 +253,23 @@ def prefix(fill_cache: bool = True) -> PagedBatch:
     return build_batch("prefix", "prefill", 5, c, n, 16, 8, 128, fill_cache=fill_cache, rng=rng)
 
 
+def mixed(fill_cache: bool = True) -> PagedBatch:
+    """One engine step of chunked prefill mixed with decode: 48 decode rows
+    (one new token, contexts ~ U[128, 2048]) and 8 prompt chunks of
+    U[256, 1024] new tokens after U[0, 2048] cached ones, 16 q / 8 kv heads,
+    D=128, served by one prefill launch."""
+    rng = np.random.default_rng(6)
+    dec_ctx = rng.integers(128, 2048, size=48, endpoint=True)
+    chunk_new = rng.integers(256, 1024, size=8, endpoint=True)
+    chunk_cached = rng.integers(0, 2048, size=8, endpoint=True)
+    cached = np.concatenate([dec_ctx - 1, chunk_cached])
+    new = np.concatenate([np.ones(48, np.int64), chunk_new])
+    return build_batch("mixed", "prefill", 6, cached, new, 16, 8, 128, fill_cache=fill_cache,
+                       rng=rng)
+
+
 WORKLOADS = {"tiny": tiny, "decode": decode, "longdecode": longdecode, "prefill": prefill,
-             "prefix": prefix}
+             "prefix": prefix, "mixed": mixed}
 
 
 def sample_rows(rng: np.random.Generator, batch: PagedBatch, per_seq: int) -> np.ndarray:
