@@ -9,9 +9,11 @@
 //
 // Design (GB300): HBM-bound streaming, 16 bytes in and 64 bytes out per 32
 // weights.  A persistent grid (SMs x 8 CTAs of 256 threads) walks 32-weight
-// chunks: one 16-byte streaming load of four words, one scale, 32 products in
-// fp32 (exact: |s4| <= 8 times a bf16 needs at most 12 significant bits),
-// each rounded once to bf16, and two 32-byte (or four 16-byte) stores.
+// chunks: one 16-byte streaming load of four words, one scale, 32 products
+// in bf16 pairs (u - 8 is exact in bf16; the multiply rounds the exact
+// product once to nearest even, as rounding an fp32 product would: that
+// product needs at most 12 significant bits), and two 32-byte (or four
+// 16-byte) stores.
 #include "host_common.h"
 #include "pkv_common.cuh"
 
@@ -36,18 +38,39 @@ __device__ __forceinline__ void st_v8(void *p, const uint32_t (&w)[8]) {
 }
 
 // Eight weights of one word, as four packed bf16 pairs (lower index in the
-// low half).  The nibble u becomes float exactly through the bit pattern
-// 0x4B000000 | u (= 2^23 + u); subtracting 2^23 + 8 gives u - 8 exactly.
-__device__ __forceinline__ void dequant_word(uint32_t word, float scale, uint32_t *out4) {
-  constexpr float kBias = 8388616.0f;  // 2^23 + 8
+// low half).  (word >> 4j) & 0x000F000F | 0x43004300 is the bf16 pair
+// (128 + u_j, 128 + u_{j+4}) exactly (bf16 holds every integer up to 256);
+// subtracting the pair (136, 136) gives (u - 8) exactly, and one bf16x2
+// multiply by the scale rounds the exact product once to nearest even.
+// Byte permutes then put the pairs in element order (0,1) (2,3) (4,5) (6,7).
+__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+
+__device__ __forceinline__ void dequant_word(uint32_t word, uint32_t scale2, uint32_t *out4) {
+  constexpr uint32_t kBias = 0x43084308u;  // bf16 pair (136, 136)
+  uint32_t r[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t u0 = (word >> (8 * i)) & 0xFu;
-    const uint32_t u1 = (word >> (8 * i + 4)) & 0xFu;
-    const float f0 = (__uint_as_float(0x4B000000u | u0) - kBias) * scale;
-    const float f1 = (__uint_as_float(0x4B000000u | u1) - kBias) * scale;
-    out4[i] = pack_bf16x2(f0, f1);
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t x = ((word >> (4 * j)) & 0x000F000Fu) | 0x43004300u;  // (128+u_j, 128+u_{j+4})
+    r[j] = bf16x2_mul(bf16x2_sub(x, kBias), scale2);
   }
+  out4[0] = prmt(r[0], r[1], 0x5410u);  // (w0, w1)
+  out4[1] = prmt(r[2], r[3], 0x5410u);  // (w2, w3)
+  out4[2] = prmt(r[0], r[1], 0x7632u);  // (w4, w5)
+  out4[3] = prmt(r[2], r[3], 0x7632u);  // (w6, w7)
 }
 
 __global__ void __launch_bounds__(kThreads)
@@ -59,8 +82,8 @@ __global__ void __launch_bounds__(kThreads)
     const int64_t row = c / chunks_per_row;
     const int64_t cir = c - row * chunks_per_row;  // chunk in row: 32 weights
     const uint4 w = ld_stream_u4(packed + c * 4);
-    const float scale =
-        __uint_as_float((uint32_t)__ldg(scales + row * groups_per_row + cir / 4) << 16);
+    const uint32_t sc = __ldg(scales + row * groups_per_row + cir / 4);
+    const uint32_t scale = sc | (sc << 16);  // the scale in both halves
     uint32_t o[16];
     dequant_word(w.x, scale, o);
     dequant_word(w.y, scale, o + 4);
