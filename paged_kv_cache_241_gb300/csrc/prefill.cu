@@ -16,17 +16,17 @@
 //    sequence's K/V from L2.  All roles run across unit boundaries: the next
 //    unit's Q/K loads and first MMAs overlap this unit's last softmax and
 //    epilogue.  The two heads of a unit share every K/V tile.
-//  * Warp 0 fetches units (passing them to the other roles through a small
-//    shared ring) and issues TMA for Q and K; the last-but-one warp issues
-//    TMA for V: 128B-swizzled 4-D boxes {64 dims, 1 head, 64 tokens, 1 block}
-//    of 64-key tiles through the block table.
+//  * Warp 0 fetches and decodes units (passing them to the other roles
+//    through a small shared ring) and issues TMA for Q and K; the
+//    last-but-one warp issues TMA for V: 128B-swizzled 4-D boxes {64 dims,
+//    1 head, 64 tokens, 1 block} of 64-key tiles through the block table.
 //  * Warp 1 issues S_h = Q_h K^T (tcgen05.mma, M=128, N=64, fp32 in tensor
-//    memory); the last warp issues O_h += P_h V (M=128, N=D, P from tensor
-//    memory, V MN-major).  Two issuers keep the tensor pipe fed while either
-//    waits on a barrier.
+//    memory, two buffers per head); the last warp issues O_h += P_h V
+//    (M=128, N=D, P from tensor memory, V MN-major).  Two issuers keep the
+//    tensor pipe fed while either waits on a barrier.
 //  * Warps 2.. (one 4-warp group per head, one thread per query row) read S,
 //    apply the causal mask offset by the cached length, run the online
-//    softmax in fp32 (log2 domain), write P as bf16 into tensor memory,
+//    softmax in fp32 (log2 domain), write P as bf16 over the S it came from,
 //    rescale O when the row max grows, and finally normalise O and store
 //    bf16 rows.
 #include <math.h>
@@ -139,27 +139,28 @@ struct PrefillLayout {
   static constexpr int v = k + kKStages * kKVBytes;
   static constexpr int bars = v + kVStages * kKVBytes;
   // barriers: q_full, q_empty, k_full[SK], v_full[SV], k_empty[SK], v_empty[SV],
-  // s_full[NH], s_free[NH], p_full[NH][2], p_free[NH][2], o_done[NH],
-  // o_free[NH], unit_full[U], unit_empty[U], drain
+  // s_full[NH][2], p_full[NH][2], p_free[NH][2], o_free[NH], unit_full[U],
+  // unit_empty[U], drain
   static_assert(kKStages >= 2 && kVStages >= 2, "rings too shallow");
   static constexpr int kNumBars =
-      2 + 2 * kKStages + 2 * kVStages + 8 * NH + 2 * kUnitSlots + 1;
+      2 + 2 * kKStages + 2 * kVStages + 7 * NH + 2 * kUnitSlots + 1;
   static constexpr int misc = bars + kNumBars * 8;  // tmem address, abort flag, unit ring
-  static constexpr int total = misc + 8 + 4 * kUnitSlots;
-  static constexpr int kCols = NH * D + 2 * NH * BN;  // per head: O, one S, two P buffers
+  static constexpr int ring = misc + 8;
+  static constexpr int total = ring + (int)sizeof(Unit) * kUnitSlots;
+  static constexpr int kCols = NH * D + 2 * NH * BN;  // per head: O and two S/P buffers
   static constexpr int kTmemCols = kCols <= 128 ? 128 : (kCols <= 256 ? 256 : 512);
 };
 
-// Tensor-memory columns (lane = query row): O_h (fp32) at kO + h*D; S_h
-// (fp32) at kS + h*BN; the two P buffers of head h (bf16 pairs, the A
-// operand of P.V) at kP + (2h + b)*BN/2, b = tile index & 1.  S is single
-// buffered: the softmax releases it as soon as it is in registers, so the
-// next S is computed while the softmax of this tile runs.
+// Tensor-memory columns (lane = query row): O_h (fp32) at kO + h*D, and two
+// S buffers per head at kS + (2h + b)*BN, b = tile index & 1.  Tile g's S_h
+// (fp32) goes to buffer g & 1; the softmax reads it into registers and
+// writes P_h (bf16 pairs, the A operand of P.V) over its first BN/2 columns.
+// So S of tile g + 1 is computed while the softmax of tile g runs, and S of
+// tile g + 2 waits only for the P.V of tile g.
 template <int D, int NH>
 struct TmemCols {
   static constexpr uint32_t kO = 0;
   static constexpr uint32_t kS = NH * D;
-  static constexpr uint32_t kP = NH * D + NH * BN;
 };
 
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
@@ -180,7 +181,6 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
   constexpr int kVStages = L::kVStages;
   constexpr uint32_t kOCol = TmemCols<D, NH>::kO;
   constexpr uint32_t kSCol = TmemCols<D, NH>::kS;
-  constexpr uint32_t kPCol = TmemCols<D, NH>::kP;
   constexpr int kVWarp = 2 + 4 * NH;   // V producer warp (after the softmax warpgroups)
   constexpr int kPVWarp = 3 + 4 * NH;  // P.V MMA issuer
 
@@ -198,18 +198,16 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
   uint64_t *v_full = k_full + kKStages;
   uint64_t *k_empty = v_full + kVStages;
   uint64_t *v_empty = k_empty + kKStages;
-  uint64_t *s_full = v_empty + kVStages;    // [NH]
-  uint64_t *s_free = s_full + NH;           // [NH]: the softmax has S in registers
-  uint64_t *p_full = s_free + NH;           // [NH][2]
-  uint64_t *p_free = p_full + 2 * NH;       // [NH][2]: P.V has read that P buffer
-  uint64_t *o_done = p_free + 2 * NH;       // [NH]
-  uint64_t *o_free = o_done + NH;           // [NH]: the epilogue has read O
+  uint64_t *s_full = v_empty + kVStages;    // [NH][2]: S in buffer b
+  uint64_t *p_full = s_full + 2 * NH;       // [NH][2]: P written over it
+  uint64_t *p_free = p_full + 2 * NH;       // [NH][2]: that P.V is done (O updated, buffer free)
+  uint64_t *o_free = p_free + 2 * NH;       // [NH]: the epilogue has read O
   uint64_t *unit_full = o_free + NH;        // [kUnitSlots]
   uint64_t *unit_empty = unit_full + kUnitSlots;
   uint64_t *drain = unit_empty + kUnitSlots;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::misc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::misc + 4);
-  volatile int *unit_ring = reinterpret_cast<volatile int *>(smem + L::misc + 8);
+  Unit *unit_ring = reinterpret_cast<Unit *>(smem + L::ring);  // decoded units; s < 0 ends
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -226,14 +224,12 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
       mbar_init(&v_empty[i], 1);
     }
     for (int h = 0; h < NH; ++h) {
-      mbar_init(&s_full[h], 1);
-      mbar_init(&s_free[h], 4);  // the 4 warps of the head's softmax group
       for (int b = 0; b < 2; ++b) {
+        mbar_init(&s_full[2 * h + b], 1);
         mbar_init(&p_full[2 * h + b], 128);  // one softmax warpgroup per head
         mbar_init(&p_free[2 * h + b], 1);
       }
-      mbar_init(&o_done[h], 1);
-      mbar_init(&o_free[h], 4);
+      mbar_init(&o_free[h], 4);  // the 4 warps of the head's softmax group
     }
     // Unit ring readers: V producer, both MMA issuers, every softmax warp.
     for (int i = 0; i < kUnitSlots; ++i) {
@@ -259,13 +255,11 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
   auto next_unit = [&](int &iu, Unit &u) -> bool {
     const int slot = iu % kUnitSlots;
     if (!warp_wait(&unit_full[slot], (iu / kUnitSlots) & 1, abort_flag)) return false;
-    const int idx = unit_ring[slot];
+    u = unit_ring[slot];
     __syncwarp();
     if (lane == 0) mbar_arrive(&unit_empty[slot]);
     ++iu;
-    if (idx < 0) return false;
-    decode_unit<NH>((unsigned)idx, p, u);
-    return true;
+    return u.s >= 0;
   };
 
   if (warp == 0 || warp == kVWarp) {
@@ -291,40 +285,42 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
       Unit u;
       bool have;
       if (is_k) {
-        // Fetch the next unit with work and publish it to the ring.  A unit
-        // without work means the rest of its sequence's units have none
-        // either (later tiles, or an empty or inconsistent sequence): move the
-        // shared counter to the next sequence instead of taking them one by one.
-        int idx = -1;
+        // Fetch and decode the next unit with work and publish it to the
+        // ring, so the other roles start a unit without reading the
+        // sequence lengths themselves.  A unit without work means the rest of
+        // its sequence's units have none either (later tiles, or an empty or
+        // inconsistent sequence): move the shared counter to the next
+        // sequence instead of taking them one by one.
+        have = false;
         if (lane == 0) {
           const unsigned int per_seq = (unsigned)(p.q_tiles * (p.num_q_heads / NH));
           for (;;) {
             const unsigned int i = atomicAdd(&p.ws->next_unit, 1u);
             if (i >= p.num_units) break;
             if (decode_unit<NH>(i, p, u)) {
-              idx = (int)i;
+              have = true;
               break;
             }
             atomicMax(&p.ws->next_unit, (i / per_seq + 1) * per_seq);
           }
+          if (!have) u.s = -1;
         }
-        idx = __shfl_sync(0xffffffffu, idx, 0);
         const int slot = iu % kUnitSlots;
         if (iu >= kUnitSlots)
           ok = warp_wait(&unit_empty[slot], ((iu / kUnitSlots) - 1) & 1, abort_flag);
         if (!ok) break;
         if (lane == 0) {
-          unit_ring[slot] = idx;
-          mbar_arrive(&unit_full[slot]);
+          unit_ring[slot] = u;
+          mbar_arrive(&unit_full[slot]);  // (release: orders the stores above)
         }
         ++iu;
-        have = idx >= 0;
-        if (have) decode_unit<NH>((unsigned)idx, p, u);
+        have = __shfl_sync(0xffffffffu, have ? 1 : 0, 0) != 0;
+        if (!have) break;
       } else {
         have = next_unit(iu, u);
       }
       if (!have) break;
-      if (lane == 0) {
+      if (lane == 0) {  // (only lane 0 of warp 0 holds the decoded unit)
         if (is_k) {
           // Q of this unit once the previous unit's S MMAs are done with Q.
           if (iu >= 2) ok = mbar_wait_bounded(q_empty, (iu - 2) & 1, abort_flag);
@@ -395,18 +391,19 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
       while (ok && next_unit(iu, u)) {
         if (lane == 0) {
           ok = mbar_wait_bounded(q_full, (iu - 1) & 1, abort_flag);
-          // Per tile: S_h for every head once K is in and the softmax has
-          // the previous S_h in registers.
+          // Per tile: S_h for every head into buffer g & 1 once K is in
+          // and the P.V two tiles back (which read P from that buffer) is done.
           for (int jt = 0; jt < u.n_kv && ok; ++jt, ++g) {
             const int st = g % kKStages;
             ok = mbar_wait_bounded(&k_full[st], (g / kKStages) & 1, abort_flag);
             const uint64_t dk_st = dk + (uint64_t)((st * L::kKVBytes) >> 4);
+            const int b = g & 1;
 #pragma unroll
             for (int h = 0; h < NH && ok; ++h) {
-              if (g >= 1) ok = mbar_wait_bounded(&s_free[h], (g - 1) & 1, abort_flag);
+              if (g >= 2) ok = mbar_wait_bounded(&p_free[2 * h + b], ((g - 2) >> 1) & 1, abort_flag);
               if (!ok) break;
               tc_fence_after_sync();
-              const uint32_t d = tmem + kSCol + h * BN;
+              const uint32_t d = tmem + kSCol + (2 * h + b) * BN;
 #pragma unroll
               for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t off = (kk & 3) * 32;
@@ -414,7 +411,7 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
                           dk_st + (uint64_t)(((kk / 4) * BN * 128 + off) >> 4), idesc_s,
                           kk > 0 ? 1u : 0u);
               }
-              umma_commit(&s_full[h]);
+              umma_commit(&s_full[2 * h + b]);
             }
             if (ok) umma_commit(&k_empty[st]);
           }
@@ -429,7 +426,7 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
       while (ok && next_unit(iu, u)) {
         if (lane == 0) {
           // Per tile, in head order: O_h += P_h V (P from tensor memory) once V
-          // is in and the head's P is written; then the P buffer and the V
+          // is in and the head's P is written; then the S/P buffer and the V
           // slot are released.  A unit's first P.V overwrites O_h, so it also
           // waits until the previous unit's epilogue has read O_h.  Head order
           // keeps every head's last P.V behind warpgroup 0, which clears the V
@@ -445,13 +442,12 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
                 ok = mbar_wait_bounded(&o_free[h], (iu - 2) & 1, abort_flag);
               if (!ok) break;
               tc_fence_after_sync();
-              const uint32_t pa = tmem + kPCol + (2 * h + (g & 1)) * (BN / 2);
+              const uint32_t pa = tmem + kSCol + (2 * h + (g & 1)) * BN;
 #pragma unroll
               for (int kk = 0; kk < BN / 16; ++kk)
                 umma_bf16_tmem_a(tmem + kOCol + h * D, pa + kk * 8,
                                  dv_st + (uint64_t)((kk * 16 * 128) >> 4), idesc_o,
                                  (jt > 0 || kk > 0) ? 1u : 0u);
-              umma_commit(&o_done[h]);
               umma_commit(&p_free[2 * h + (g & 1)]);
             }
             if (ok) umma_commit(&v_empty[pst]);
@@ -485,16 +481,13 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
       float l_run = 0.f;
       for (int jt = 0; jt < u.n_kv && ok; ++jt, ++g) {
         const int key0 = jt * BN;
-        ok = warp_wait(&s_full[h], g & 1, abort_flag);
+        const uint32_t sp = tmem + lane_base + kSCol + (2 * h + (g & 1)) * BN;  // S, then P
+        ok = warp_wait(&s_full[2 * h + (g & 1)], (g >> 1) & 1, abort_flag);
         if (!ok) break;
         tc_fence_after_sync();
         float sv[BN];
         static_assert(BN == 64, "S is read with one 64-column TMEM load");
-        tmem_load64(tmem + lane_base + kSCol + h * BN, sv);
-        // S is in registers: the S buffer may take the next S.
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s_free[h]);
+        tmem_load64(sp, sv);
         // Tile max of the scaled logits over this row's visible keys (4-way tree).
         const bool full_row = key0 + BN - 1 <= key_limit;
         float mt;
@@ -562,16 +555,13 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
           }
           rs = (r0 + r1) + (r2 + r3);
         }
-        // P buffer g & 1 is free once the P.V two tiles back has read it.
-        if (g >= 2) {
-          ok = warp_wait(&p_free[2 * h + (g & 1)], ((g - 2) >> 1) & 1, abort_flag);
-          if (!ok) break;
-        }
         if (jt > 0 && __any_sync(0xffffffffu, alpha < 1.f)) {
           // O is rescaled once the previous P.V has landed in it (the next
-          // waits for this tile's P).  The P.V two tiles back is complete
-          // (waited for above), so the parity wait cannot alias.
-          ok = warp_wait(&o_done[h], (g - 1) & 1, abort_flag);
+          // waits for this tile's P).  Waited for through that tile's buffer:
+          // its use before (tile g - 3) was done before S of tile g - 1 was
+          // computed, and its next use needs this tile's P, so the parity
+          // wait cannot alias.
+          ok = warp_wait(&p_free[2 * h + ((g - 1) & 1)], ((g - 1) >> 1) & 1, abort_flag);
           if (!ok) break;
           tc_fence_after_sync();
 #pragma unroll 1
@@ -603,24 +593,24 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
           }
           fence_proxy_async_smem();  // the MMA reads these rows through the async proxy
         }
-        // P (bf16 pairs) into P buffer g & 1.
+        // P (bf16 pairs) over the first half of this tile's S buffer.
         {
           float pw[BN / 2];
 #pragma unroll
           for (int i = 0; i < BN / 2; ++i)
             pw[i] = __uint_as_float(pack_bf16x2(sv[2 * i], sv[2 * i + 1]));
           static_assert(BN / 2 == 32, "P is written with one 32-column TMEM store");
-          tmem_store32(tmem + lane_base + kPCol + (2 * h + (g & 1)) * (BN / 2), pw);
+          tmem_store32(sp, pw);
         }
         tc_fence_before_sync();
         mbar_arrive(&p_full[2 * h + (g & 1)]);
       }
       if (!ok) break;
       // Epilogue: O / l -> bf16 rows, once the unit's last P.V (tile g - 1) is
-      // in O.  Waited for through its P buffer's barrier: that buffer's
-      // earlier use (tile g - 3) was waited for and its next use is not yet
-      // published, so the parity wait cannot alias.  (o_done could: it may be
-      // a phase further on than the wait assumes.)
+      // in O.  Waited for through its buffer's barrier: that buffer's earlier
+      // use (tile g - 3) was done before S of tile g - 1, and its next use
+      // needs a P this warpgroup has not yet written, so the parity wait
+      // cannot alias.
       ok = warp_wait(&p_free[2 * h + ((g - 1) & 1)], ((g - 1) >> 1) & 1, abort_flag);
       if (!ok) break;
       tc_fence_after_sync();
