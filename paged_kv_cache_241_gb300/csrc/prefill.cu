@@ -163,6 +163,49 @@ struct TmemCols {
   static constexpr uint32_t kS = NH * D;
 };
 
+// Paired fp32 arithmetic (one instruction for two lanes of a register pair):
+// the same results as the scalar operations, half the instructions.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+// Maximum of three (one instruction).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
   const bool ok = mbar_wait_bounded(bar, parity, abort);
   return __all_sync(0xffffffffu, ok);
@@ -472,6 +515,49 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
     int iu = 0, g = 0;
     bool ok = true;
     Unit u;
+    // Epilogue of a unit (rows from query row e_row0, e_rows of them valid,
+    // heads from e_h): O / l -> bf16 rows once its last P.V (tile g_last) is
+    // in O.  Run after the next unit's first P is published, so the wait for
+    // that P.V overlaps the first softmax tile of the next unit.  Waited for
+    // through g_last's buffer barrier: its use before (tile g_last - 2) was
+    // done before S of g_last was computed, and its next use needs a P this
+    // warpgroup has not yet written, so the parity wait cannot alias.
+    auto epilogue = [&](int e_row0, int e_rows, int e_h, float l_e, int g_last) -> bool {
+      if (!warp_wait(&p_free[2 * h + (g_last & 1)], (g_last >> 1) & 1, abort_flag)) return false;
+      tc_fence_after_sync();
+      const float inv = 1.f / l_e;
+      uint16_t *dst = p.out + ((int64_t)(e_row0 + row) * p.num_q_heads + e_h + h) * D;
+#pragma unroll 1
+      for (int half = 0; half < D / 64; ++half) {
+        float ov[64];
+        tmem_load64(tmem + lane_base + kOCol + h * D + half * 64, ov);
+        if (row < e_rows) {
+#pragma unroll
+          for (int i = 0; i < 64; i += 16) {
+            uint32_t w[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float2 o2 = mul2(make_float2(ov[i + 2 * e], ov[i + 2 * e + 1]), make_float2(inv, inv));
+              w[e] = pack_bf16x2(o2.x, o2.y);
+            }
+            if (p.out_32b) {
+              st_global_v8(dst + half * 64 + i, w);
+            } else {
+              *reinterpret_cast<uint4 *>(dst + half * 64 + i) = make_uint4(w[0], w[1], w[2], w[3]);
+              *reinterpret_cast<uint4 *>(dst + half * 64 + i + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+            }
+          }
+        }
+      }
+      // O is read: the next unit's first P.V may overwrite it.
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&o_free[h]);
+      return true;
+    };
+    bool pending = false;  // a unit's epilogue is still to run
+    int e_row0 = 0, e_rows = 0, e_h = 0, e_g = 0;
+    float e_l = 0.f;
     while (ok && next_unit(iu, u)) {
       const int key_limit = min(u.c + u.q0 + row, u.len_k - 1);  // last key this row may see
       // Running max in log2 units.  It is only raised (and O rescaled) when a
@@ -496,11 +582,11 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
           if (qs >= 0.f) {
             if (full_row) {
 #pragma unroll
-              for (int i = 0; i < BN; i += 4) {
-                e0 = fmaxf(e0, sv[i]);
-                e1 = fmaxf(e1, sv[i + 1]);
-                e2 = fmaxf(e2, sv[i + 2]);
-                e3 = fmaxf(e3, sv[i + 3]);
+              for (int i = 0; i < BN; i += 8) {
+                e0 = max3(e0, sv[i], sv[i + 1]);
+                e1 = max3(e1, sv[i + 2], sv[i + 3]);
+                e2 = max3(e2, sv[i + 4], sv[i + 5]);
+                e3 = max3(e3, sv[i + 6], sv[i + 7]);
               }
             } else {
 #pragma unroll
@@ -529,17 +615,23 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
         {
           float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
           if (full_row) {
+            const float2 q2 = make_float2(qs, qs), nm2 = make_float2(-m_ref, -m_ref);
+            float2 r01 = make_float2(0.f, 0.f), r23 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int i = 0; i < BN; i += 4) {
-              sv[i] = fast_exp2(fmaf(sv[i], qs, -m_ref));
-              sv[i + 1] = fast_exp2(fmaf(sv[i + 1], qs, -m_ref));
-              sv[i + 2] = fast_exp2(fmaf(sv[i + 2], qs, -m_ref));
-              sv[i + 3] = fast_exp2(fmaf(sv[i + 3], qs, -m_ref));
-              r0 += sv[i];
-              r1 += sv[i + 1];
-              r2 += sv[i + 2];
-              r3 += sv[i + 3];
+              const float2 x01 = fma2(make_float2(sv[i], sv[i + 1]), q2, nm2);
+              const float2 x23 = fma2(make_float2(sv[i + 2], sv[i + 3]), q2, nm2);
+              sv[i] = fast_exp2(x01.x);
+              sv[i + 1] = fast_exp2(x01.y);
+              sv[i + 2] = fast_exp2(x23.x);
+              sv[i + 3] = fast_exp2(x23.y);
+              r01 = add2(r01, make_float2(sv[i], sv[i + 1]));
+              r23 = add2(r23, make_float2(sv[i + 2], sv[i + 3]));
             }
+            r0 = r01.x;
+            r1 = r01.y;
+            r2 = r23.x;
+            r3 = r23.y;
           } else {
 #pragma unroll
             for (int i = 0; i < BN; i += 4) {
@@ -570,7 +662,11 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
             const uint32_t oa = tmem + lane_base + kOCol + h * D + cc * 32;
             tmem_load32(oa, ov);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) ov[i] *= alpha;
+            for (int i = 0; i < 32; i += 2) {
+              const float2 o2 = mul2(make_float2(ov[i], ov[i + 1]), make_float2(alpha, alpha));
+              ov[i] = o2.x;
+              ov[i + 1] = o2.y;
+            }
             tmem_store32(oa, ov);
           }
         }
@@ -604,43 +700,20 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
         }
         tc_fence_before_sync();
         mbar_arrive(&p_full[2 * h + (g & 1)]);
-      }
-      if (!ok) break;
-      // Epilogue: O / l -> bf16 rows, once the unit's last P.V (tile g - 1) is
-      // in O.  Waited for through its buffer's barrier: that buffer's earlier
-      // use (tile g - 3) was done before S of tile g - 1, and its next use
-      // needs a P this warpgroup has not yet written, so the parity wait
-      // cannot alias.
-      ok = warp_wait(&p_free[2 * h + ((g - 1) & 1)], ((g - 1) >> 1) & 1, abort_flag);
-      if (!ok) break;
-      tc_fence_after_sync();
-      const float inv = 1.f / l_run;
-      uint16_t *dst =
-          p.out + ((int64_t)(u.q_begin + u.q0 + row) * p.num_q_heads + u.h_first + h) * D;
-#pragma unroll 1
-      for (int half = 0; half < D / 64; ++half) {
-        float ov[64];
-        tmem_load64(tmem + lane_base + kOCol + h * D + half * 64, ov);
-        if (row < u.rows_valid) {
-#pragma unroll
-          for (int i = 0; i < 64; i += 16) {
-            uint32_t w[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(ov[i + 2 * e] * inv, ov[i + 2 * e + 1] * inv);
-            if (p.out_32b) {
-              st_global_v8(dst + half * 64 + i, w);
-            } else {
-              *reinterpret_cast<uint4 *>(dst + half * 64 + i) = make_uint4(w[0], w[1], w[2], w[3]);
-              *reinterpret_cast<uint4 *>(dst + half * 64 + i + 8) = make_uint4(w[4], w[5], w[6], w[7]);
-            }
-          }
+        if (pending) {  // the previous unit's epilogue, after this unit's first P
+          pending = false;
+          ok = epilogue(e_row0, e_rows, e_h, e_l, e_g);
         }
       }
-      // O is read: the next unit's first P.V may overwrite it.
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&o_free[h]);
+      if (!ok) break;
+      pending = true;
+      e_row0 = u.q_begin + u.q0;
+      e_rows = u.rows_valid;
+      e_h = u.h_first;
+      e_l = l_run;
+      e_g = g - 1;
     }
+    if (ok && pending) ok = epilogue(e_row0, e_rows, e_h, e_l, e_g);
     tc_fence_before_sync();
   }
 
