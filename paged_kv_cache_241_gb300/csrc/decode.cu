@@ -24,8 +24,9 @@
 //    softmax statistics of the item.  Phase 3: P.V with each lane owning D/32
 //    output dims.
 //  * Each item writes a partial (max, sum, unnormalised output) to the
-//    workspace; the last item of a (sequence, kv head) to finish (atomic
-//    ticket, no spinning) merges the partials and writes bf16.  A sequence
+//    workspace; a merge kernel, launched as a programmatic dependent of this
+//    grid (it waits for the grid's completion), combines each multi-block
+//    (sequence, kv head)'s partials in parallel and writes bf16.  A sequence
 //    that fits one block skips the workspace.
 #include <math.h>
 
