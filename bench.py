@@ -322,7 +322,11 @@ class Arm:
                                         b.scale, workspace=self.pws, dev_status=self.status)
 
     def run(self, steps, warmup):
-        """Time `steps` steps; returns (total ms, mean attention-kernel ms, mean store ms)."""
+        """Time `steps` steps; returns (total ms, mean attention-kernel ms, mean store ms).
+
+        The whole-job total comes from a loop with events only around it; the
+        per-kernel means from a second loop with events around each call
+        (which themselves take time between the launches)."""
         import torch
 
         stream = torch.cuda.current_stream()
@@ -330,11 +334,17 @@ class Arm:
             self.store(i)
             self.attend(i)
         torch.cuda.synchronize()
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-               torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record(stream)
+        for i in range(steps):
+            self.store(i)
+            self.attend(i)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        total = t0.elapsed_time(t1)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+               torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
         for i in range(steps):
             e0, e1, e2 = ev[i]
             e0.record(stream)
@@ -342,9 +352,7 @@ class Arm:
             e1.record(stream)
             self.attend(i)
             e2.record(stream)
-        t1.record(stream)
         torch.cuda.synchronize()
-        total = t0.elapsed_time(t1)
         store_ms = sum(e0.elapsed_time(e1) for e0, e1, _ in ev) / steps
         attn_ms = sum(e1.elapsed_time(e2) for _, e1, e2 in ev) / steps
         if int(self.status.item()) != 0:
