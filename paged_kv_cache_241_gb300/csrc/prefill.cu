@@ -40,6 +40,7 @@ namespace {
 constexpr int BM = 128;  // query rows per tile (MMA M)
 constexpr int BN = 64;   // keys per tile
 constexpr int kUnitSlots = 4;  // depth of the shared ring of fetched units
+constexpr int kMaxSorted = 256;  // sequences ordered longest-first in shared memory (more: as given)
 // Warp 0: unit fetcher + Q/K TMA producer; warp 1: S = QK^T MMA issuer; then
 // one 4-warp softmax group per head; then the V TMA producer and the P.V MMA
 // issuer.
@@ -64,6 +65,7 @@ struct PrefillParams {
   int64_t num_blocks;
   int64_t total_q;
   int num_seqs;
+  int sorted;        // num_seqs <= kMaxSorted: units follow the longest-first sequence order
   int num_q_heads;
   int num_kv_heads;
   int block_size;
@@ -88,15 +90,18 @@ struct Unit {
 };
 
 // Unit index -> unit (sequence-major, heaviest tile of a sequence first, head
-// groups innermost).  False when the index has no work (a tile past a short
-// prompt) or its lengths are inconsistent (then PKV_DEV_BAD_SEQLEN is set).
+// groups innermost; sequences longest context first when `order` is in use).
+// False when the index has no work (a tile past a short prompt) or its
+// lengths are inconsistent (then PKV_DEV_BAD_SEQLEN is set).
 template <int NH>
-__device__ bool decode_unit(unsigned int idx, const PrefillParams &p, Unit &u) {
+__device__ bool decode_unit(unsigned int idx, const PrefillParams &p, const uint32_t *order,
+                            Unit &u) {
   const int HG = p.num_q_heads / NH;
   const int hg = (int)(idx % (unsigned)HG);
   idx /= (unsigned)HG;
   const int tr = (int)(idx % (unsigned)p.q_tiles);
-  const int s = (int)(idx / (unsigned)p.q_tiles);
+  const int rank = (int)(idx / (unsigned)p.q_tiles);
+  const int s = p.sorted ? 0xFFFF - (int)(order[rank] & 0xFFFFu) : rank;
   const int q_begin = p.cu_q[s];
   const int n = p.cu_q[s + 1] - q_begin;
   const int len_k = p.cu_k[s + 1] - p.cu_k[s];
@@ -130,7 +135,7 @@ struct PrefillLayout {
   // Ring depths: the K/V slots that fit next to Q in 227 KiB of shared
   // memory (at most 12).  A K slot is held until its S MMAs finish, a V slot
   // until its P.V has run, so V gets the larger share.
-  static constexpr int kSlots0 = (232448 - 2048 - NH * kQBytes) / kKVBytes;
+  static constexpr int kSlots0 = (232448 - 3072 - NH * kQBytes) / kKVBytes;
   static constexpr int kSlots = kSlots0 < 12 ? kSlots0 : 12;
   static constexpr int kKStages = kSlots * 2 / 5;
   static constexpr int kVStages = kSlots - kKStages;
@@ -146,7 +151,9 @@ struct PrefillLayout {
       2 + 2 * kKStages + 2 * kVStages + 7 * NH + 2 * kUnitSlots + 1;
   static constexpr int misc = bars + kNumBars * 8;  // tmem address, abort flag, unit ring
   static constexpr int ring = misc + 8;
-  static constexpr int total = ring + (int)sizeof(Unit) * kUnitSlots;
+  static constexpr int order = ring + (int)sizeof(Unit) * kUnitSlots;  // [kMaxSorted] sort keys
+  static constexpr int total = order + 4 * kMaxSorted;
+  static_assert(total + 1024 <= 232448, "shared memory");
   static constexpr int kCols = NH * D + 2 * NH * BN;  // per head: O and two S/P buffers
   static constexpr int kTmemCols = kCols <= 128 ? 128 : (kCols <= 256 ? 256 : 512);
 };
@@ -206,6 +213,41 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   return d;
 }
 
+// Sequences longest context first (ties by index), so the longest units
+// start first and the CTAs finish together: keys (key tiles << 16 |
+// 0xFFFF - s), bitonic-sorted in descending order over the next power of two
+// (padding keys are 0 and sort last).  Every CTA sorts its own copy; all
+// threads of the CTA call this.  (Kept out of line: the kernel's loops run
+// faster with this code outside them.)
+static __device__ __noinline__ void sort_sequences(const PrefillParams &p, uint32_t *order) {
+  int n2 = 1;
+  while (n2 < p.num_seqs) n2 <<= 1;
+  for (int i = threadIdx.x; i < n2; i += blockDim.x) {
+    uint32_t key = 0;
+    if (i < p.num_seqs) {
+      const int lk = p.cu_k[i + 1] - p.cu_k[i];
+      const uint32_t cost = lk <= 0 ? 0u : min((uint32_t)((lk + BN - 1) / BN), 0xFFFFu);
+      key = (cost << 16) | (uint32_t)(0xFFFF - i);
+    }
+    order[i] = key;
+  }
+  __syncthreads();
+  for (int k = 2; k <= n2; k <<= 1)
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < n2; i += blockDim.x) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const uint32_t a = order[i], b = order[ixj];
+          if (((i & k) == 0) ? (a < b) : (a > b)) {
+            order[i] = b;
+            order[ixj] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+}
+
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
   const bool ok = mbar_wait_bounded(bar, parity, abort);
   return __all_sync(0xffffffffu, ok);
@@ -251,6 +293,7 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::misc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::misc + 4);
   Unit *unit_ring = reinterpret_cast<Unit *>(smem + L::ring);  // decoded units; s < 0 ends
+  uint32_t *order = reinterpret_cast<uint32_t *>(smem + L::order);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -287,6 +330,7 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
     tmem_alloc(tmem_slot, L::kTmemCols);
     tmem_relinquish();
   }
+  if (p.sorted) sort_sequences(p, order);
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
@@ -340,7 +384,7 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
           for (;;) {
             const unsigned int i = atomicAdd(&p.ws->next_unit, 1u);
             if (i >= p.num_units) break;
-            if (decode_unit<NH>(i, p, u)) {
+            if (decode_unit<NH>(i, p, order, u)) {
               have = true;
               break;
             }
@@ -805,6 +849,7 @@ extern "C" pkv_status pkv_paged_prefill_attn(uint16_t *out, const uint16_t *q,
   prm.num_blocks = num_blocks;
   prm.total_q = total_q;
   prm.num_seqs = num_seqs;
+  prm.sorted = num_seqs <= kMaxSorted ? 1 : 0;
   prm.num_q_heads = num_q_heads;
   prm.num_kv_heads = num_kv_heads;
   prm.block_size = block_size;

@@ -151,3 +151,41 @@ def test_prefill_output_only_16_byte_aligned(lib):
                                      b.cu_seqlens_k, b.scale)
     assert_close(out.double().cpu().numpy(), want, "prefill, 16-byte aligned out")
     assert torch.count_nonzero(buf[:8]) == 0
+
+
+@pytest.mark.parametrize("num_seqs", [256, 257])
+def test_prefill_many_sequences(lib, num_seqs):
+    # Up to 256 sequences the kernel orders them longest context first (sorted
+    # in shared memory); beyond that it keeps their given order.  Both paths,
+    # with many equal lengths (ties keep their index order) and one-token
+    # prompts.
+    rng = np.random.default_rng(70 + num_seqs)
+    new = [int(x) for x in rng.choice([1, 7, 40, 130], size=num_seqs)]
+    cached = [int(x) for x in rng.choice([0, 0, 256, 300], size=num_seqs)]
+    b = wl.build_batch("many", "prefill", 70 + num_seqs, cached, new, 4, 2, 128)
+    check_prefill(lib, b)
+
+
+def test_prefill_sequence_order_keeps_results(lib):
+    # The same sequences given in another order give the same rows, bit for
+    # bit: the processing order is a schedule, not part of the result.
+    cached = [0, 1024, 256, 0, 512, 0]
+    new = [300, 20, 129, 1, 64, 900]
+    b = wl.build_batch("order", "prefill", 71, cached, new, 8, 4, 128)
+    db, out = check_prefill(lib, b)
+    perm = [5, 2, 0, 4, 1, 3]
+    starts = b.cu_seqlens_q[:-1]
+    rows = torch.as_tensor(np.concatenate([np.arange(starts[s], starts[s] + new[s]) for s in perm]),
+                           device="cuda")
+    q2 = db.q[rows].contiguous()
+    bt2 = db.block_tables[torch.as_tensor(perm, device="cuda")].contiguous()
+    cu_q2 = torch.as_tensor(np.concatenate([[0], np.cumsum([new[s] for s in perm])]),
+                            dtype=torch.int32, device="cuda")
+    cu_k2 = torch.as_tensor(np.concatenate([[0], np.cumsum([new[s] + cached[s] for s in perm])]),
+                            dtype=torch.int32, device="cuda")
+    out2 = torch.empty_like(out)
+    lib.paged_prefill_attn(out2, q2, db.k_cache, db.v_cache, bt2, cu_q2, cu_k2, max(new), b.scale,
+                           dev_status=db.status)
+    torch.cuda.synchronize()
+    assert db.status_value() == 0
+    assert torch.equal(out2, out[rows])
