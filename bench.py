@@ -361,39 +361,79 @@ class Arm:
 
 
 def e2e_decode(pkv, b, dev, steps, warmup):
-    """Decode step through host buffers: per step copy the step's inputs from
-    pinned host memory, store + attend, copy the output back."""
+    """Decode step through host buffers: every step copies the step's inputs
+    from pinned host memory (one packed copy), stores + attends, and copies
+    the output back, as a serving loop would run it: the inputs of step i+1
+    are copied (own stream) while step i computes, and the output of step i
+    is read back (another stream) while step i+1 computes; device input and
+    output buffers alternate between two sets.  Returns (ms per step, H2D
+    bytes per step, D2H bytes per step)."""
     import torch
 
     t = device_batch(b, dev, b.k_cache is None, b.seed)
-    host = {k: t[k].cpu().pin_memory() for k in ("q", "k", "v", "slot_mapping", "block_tables",
-                                                   "context_lens")}
-    out_host = torch.empty((b.num_seqs, b.num_q_heads, b.head_dim), dtype=torch.bfloat16).pin_memory()
-    out = torch.empty((b.num_seqs, b.num_q_heads, b.head_dim), dtype=torch.bfloat16, device=dev)
+    names = ("q", "k", "v", "slot_mapping", "block_tables", "context_lens")
+    offs, nbytes = {}, 0
+    for k in names:  # packed layout, every input 256-byte aligned
+        offs[k] = nbytes
+        nbytes += (t[k].numel() * t[k].element_size() + 255) // 256 * 256
+    host = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    for k in names:
+        n = t[k].numel() * t[k].element_size()
+        host[offs[k]:offs[k] + n].copy_(t[k].cpu().contiguous().view(-1).view(torch.uint8))
+    stage = [torch.empty(nbytes, dtype=torch.uint8, device=dev) for _ in range(2)]
+
+    def views(buf):
+        return {k: buf[offs[k]:offs[k] + t[k].numel() * t[k].element_size()].view(t[k].dtype)
+                .view(t[k].shape) for k in names}
+
+    ins = [views(x) for x in stage]
+    shape = (b.num_seqs, b.num_q_heads, b.head_dim)
+    out = [torch.empty(shape, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    out_host = [torch.empty(shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     mtb = b.total_blocks_used
-    ws = pkv.decode_workspace(b.num_seqs, b.num_q_heads, b.num_kv_heads, b.head_dim, mtb, dev)
+    ws = [pkv.decode_workspace(b.num_seqs, b.num_q_heads, b.num_kv_heads, b.head_dim, mtb, dev)
+          for _ in range(2)]
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = out_host.numel() * out_host.element_size()
+    h2d = nbytes
+    d2h = out_host[0].numel() * out_host[0].element_size()
+    comp = torch.cuda.current_stream()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    copied = [torch.cuda.Event() for _ in range(2)]
+    computed = [torch.cuda.Event() for _ in range(2)]
+    read = [torch.cuda.Event() for _ in range(2)]
 
-    def step():
-        for k, v in host.items():
-            t[k].copy_(v, non_blocking=True)
-        pkv.paged_decode_store_attn(out, t["q"], t["k"], t["v"], t["slot_mapping"], t["k_cache"],
-                                    t["v_cache"], t["block_tables"], t["context_lens"], b.scale,
-                                    ws, mtb, status)
-        out_host.copy_(out, non_blocking=True)
+    def step(i):
+        j = i % 2
+        with torch.cuda.stream(up):
+            up.wait_event(computed[j])  # the step that last used this input set is done
+            stage[j].copy_(host, non_blocking=True)
+            copied[j].record(up)
+        comp.wait_event(copied[j])
+        comp.wait_event(read[j])  # this output buffer's previous result was read back
+        x = ins[j]
+        pkv.paged_decode_store_attn(out[j], x["q"], x["k"], x["v"], x["slot_mapping"],
+                                    t["k_cache"], t["v_cache"], x["block_tables"],
+                                    x["context_lens"], b.scale, ws[j], mtb, status)
+        computed[j].record(comp)
+        with torch.cuda.stream(down):
+            down.wait_event(computed[j])
+            out_host[j].copy_(out[j], non_blocking=True)
+            read[j].record(down)
 
-    for _ in range(warmup):
-        step()
+    for i in range(warmup):
+        step(i)
     torch.cuda.synchronize()
     s = torch.cuda.Event(enable_timing=True)
     e = torch.cuda.Event(enable_timing=True)
-    s.record()
-    for _ in range(steps):
-        step()
-    e.record()
+    s.record(comp)
+    for i in range(steps):
+        step(i)
+    for j in range(2):
+        comp.wait_event(read[j])  # the last results are back on the host
+    e.record(comp)
     torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item()):#x} in the end-to-end leg")
     ms = s.elapsed_time(e) / steps
     return ms, h2d, d2h
 
