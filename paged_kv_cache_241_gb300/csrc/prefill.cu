@@ -617,81 +617,88 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
         tc_fence_after_sync();
         float sv[BN];
         static_assert(BN == 64, "S is read with one 64-column TMEM load");
-        tmem_load64(sp, sv);
-        // Tile max of the scaled logits over this row's visible keys (4-way tree).
-        const bool full_row = key0 + BN - 1 <= key_limit;
-        float mt;
-        {
-          float e0 = -INFINITY, e1 = -INFINITY, e2 = -INFINITY, e3 = -INFINITY;
-          if (qs >= 0.f) {
-            if (full_row) {
+        float alpha = 1.f;
+        float rs = 0.f;
+        // A warp whose 32 query rows all lie past the tile's valid rows (a
+        // decode row, a prompt's ragged last tile) skips the arithmetic and
+        // the P store: those rows' outputs are never written, and P of a row
+        // only reaches that row of O.  It still takes part in every barrier.
+        const bool live = quarter * 32 < u.rows_valid;
+        if (live) {
+          tmem_load64(sp, sv);
+          // Tile max of the scaled logits over this row's visible keys (4-way tree).
+          const bool full_row = key0 + BN - 1 <= key_limit;
+          float mt;
+          {
+            float e0 = -INFINITY, e1 = -INFINITY, e2 = -INFINITY, e3 = -INFINITY;
+            if (qs >= 0.f) {
+              if (full_row) {
 #pragma unroll
-              for (int i = 0; i < BN; i += 8) {
-                e0 = max3(e0, sv[i], sv[i + 1]);
-                e1 = max3(e1, sv[i + 2], sv[i + 3]);
-                e2 = max3(e2, sv[i + 4], sv[i + 5]);
-                e3 = max3(e3, sv[i + 6], sv[i + 7]);
+                for (int i = 0; i < BN; i += 8) {
+                  e0 = max3(e0, sv[i], sv[i + 1]);
+                  e1 = max3(e1, sv[i + 2], sv[i + 3]);
+                  e2 = max3(e2, sv[i + 4], sv[i + 5]);
+                  e3 = max3(e3, sv[i + 6], sv[i + 7]);
+                }
+              } else {
+#pragma unroll
+                for (int i = 0; i < BN; ++i)
+                  if (key0 + i <= key_limit) e0 = fmaxf(e0, sv[i]);
               }
+              mt = fmaxf(fmaxf(e0, e1), fmaxf(e2, e3)) * qs;
             } else {
+              e0 = INFINITY;
 #pragma unroll
               for (int i = 0; i < BN; ++i)
-                if (key0 + i <= key_limit) e0 = fmaxf(e0, sv[i]);
-            }
-            mt = fmaxf(fmaxf(e0, e1), fmaxf(e2, e3)) * qs;
-          } else {
-            e0 = INFINITY;
-#pragma unroll
-            for (int i = 0; i < BN; ++i)
-              if (key0 + i <= key_limit) e0 = fminf(e0, sv[i]);
-            mt = e0 * qs;
-          }
-        }
-        // Key 0 is in the first tile and visible to every row, so the first tile
-        // sets a finite max (the -inf guard keeps a row with no visible key at
-        // alpha = 0 instead of NaN).
-        float alpha = 1.f;
-        if (jt == 0 || mt > m_ref + 8.f) {
-          const float m_new = fmaxf(m_ref, mt);
-          alpha = (m_ref == -INFINITY) ? 0.f : fast_exp2(m_ref - m_new);
-          m_ref = m_new;
-        }
-        float rs;
-        {
-          float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
-          if (full_row) {
-            const float2 q2 = make_float2(qs, qs), nm2 = make_float2(-m_ref, -m_ref);
-            float2 r01 = make_float2(0.f, 0.f), r23 = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int i = 0; i < BN; i += 4) {
-              const float2 x01 = fma2(make_float2(sv[i], sv[i + 1]), q2, nm2);
-              const float2 x23 = fma2(make_float2(sv[i + 2], sv[i + 3]), q2, nm2);
-              sv[i] = fast_exp2(x01.x);
-              sv[i + 1] = fast_exp2(x01.y);
-              sv[i + 2] = fast_exp2(x23.x);
-              sv[i + 3] = fast_exp2(x23.y);
-              r01 = add2(r01, make_float2(sv[i], sv[i + 1]));
-              r23 = add2(r23, make_float2(sv[i + 2], sv[i + 3]));
-            }
-            r0 = r01.x;
-            r1 = r01.y;
-            r2 = r23.x;
-            r3 = r23.y;
-          } else {
-#pragma unroll
-            for (int i = 0; i < BN; i += 4) {
-#pragma unroll
-              for (int w = 0; w < 4; ++w)
-                sv[i + w] =
-                    (key0 + i + w <= key_limit) ? fast_exp2(fmaf(sv[i + w], qs, -m_ref)) : 0.f;
-              r0 += sv[i];
-              r1 += sv[i + 1];
-              r2 += sv[i + 2];
-              r3 += sv[i + 3];
+                if (key0 + i <= key_limit) e0 = fminf(e0, sv[i]);
+              mt = e0 * qs;
             }
           }
-          rs = (r0 + r1) + (r2 + r3);
+          // Key 0 is in the first tile and visible to every row, so the first tile
+          // sets a finite max (the -inf guard keeps a row with no visible key at
+          // alpha = 0 instead of NaN).
+          if (jt == 0 || mt > m_ref + 8.f) {
+            const float m_new = fmaxf(m_ref, mt);
+            alpha = (m_ref == -INFINITY) ? 0.f : fast_exp2(m_ref - m_new);
+            m_ref = m_new;
+          }
+          {
+            float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
+            if (full_row) {
+              const float2 q2 = make_float2(qs, qs), nm2 = make_float2(-m_ref, -m_ref);
+              float2 r01 = make_float2(0.f, 0.f), r23 = make_float2(0.f, 0.f);
+#pragma unroll
+              for (int i = 0; i < BN; i += 4) {
+                const float2 x01 = fma2(make_float2(sv[i], sv[i + 1]), q2, nm2);
+                const float2 x23 = fma2(make_float2(sv[i + 2], sv[i + 3]), q2, nm2);
+                sv[i] = fast_exp2(x01.x);
+                sv[i + 1] = fast_exp2(x01.y);
+                sv[i + 2] = fast_exp2(x23.x);
+                sv[i + 3] = fast_exp2(x23.y);
+                r01 = add2(r01, make_float2(sv[i], sv[i + 1]));
+                r23 = add2(r23, make_float2(sv[i + 2], sv[i + 3]));
+              }
+              r0 = r01.x;
+              r1 = r01.y;
+              r2 = r23.x;
+              r3 = r23.y;
+            } else {
+#pragma unroll
+              for (int i = 0; i < BN; i += 4) {
+#pragma unroll
+                for (int w = 0; w < 4; ++w)
+                  sv[i + w] =
+                      (key0 + i + w <= key_limit) ? fast_exp2(fmaf(sv[i + w], qs, -m_ref)) : 0.f;
+                r0 += sv[i];
+                r1 += sv[i + 1];
+                r2 += sv[i + 2];
+                r3 += sv[i + 3];
+              }
+            }
+            rs = (r0 + r1) + (r2 + r3);
+          }
         }
-        if (jt > 0 && __any_sync(0xffffffffu, alpha < 1.f)) {
+        if (live && jt > 0 && __any_sync(0xffffffffu, alpha < 1.f)) {
           // O is rescaled once the previous P.V has landed in it (the next
           // waits for this tile's P).  Waited for through that tile's buffer:
           // its use before (tile g - 3) was done before S of tile g - 1 was
@@ -734,7 +741,7 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
           fence_proxy_async_smem();  // the MMA reads these rows through the async proxy
         }
         // P (bf16 pairs) over the first half of this tile's S buffer.
-        {
+        if (live) {
           float pw[BN / 2];
 #pragma unroll
           for (int i = 0; i < BN / 2; ++i)
