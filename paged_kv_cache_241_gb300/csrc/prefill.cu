@@ -11,9 +11,10 @@
 // Design (GB300):
 //  * Persistent: one CTA per SM takes work units (sequence, 128-query tile,
 //    pair of query heads of one GQA group) from an atomic counter in a small
-//    caller workspace, in sequence-major order (a sequence's heaviest tiles
-//    first, head groups innermost), so that concurrent units reuse a
-//    sequence's K/V from L2.  All roles run across unit boundaries: the next
+//    caller workspace, in sequence-major order (sequences longest context
+//    first, a sequence's heaviest tiles first, head groups innermost), so
+//    that concurrent units reuse a sequence's K/V from L2 and the longest
+//    units start first.  All roles run across unit boundaries: the next
 //    unit's Q/K loads and first MMAs overlap this unit's last softmax and
 //    epilogue.  The two heads of a unit share every K/V tile.
 //  * Warp 0 fetches and decodes units (passing them to the other roles
