@@ -189,3 +189,28 @@ def test_prefill_sequence_order_keeps_results(lib):
     torch.cuda.synchronize()
     assert db.status_value() == 0
     assert torch.equal(out2, out[rows])
+
+
+def test_prefill_sequence_without_new_tokens_is_skipped(lib):
+    # A sequence with cached context but no new tokens (empty query range)
+    # has no units; it still sorts among the others by its context length.
+    # The other sequences' rows equal those of the batch that includes it.
+    cached = [0, 2048, 256, 0]
+    new = [200, 64, 129, 40]
+    b = wl.build_batch("empty", "prefill", 72, cached, new, 8, 4, 128)
+    db, out = check_prefill(lib, b)
+    keep = [0, 2, 3]
+    starts = b.cu_seqlens_q[:-1]
+    rows = torch.as_tensor(np.concatenate([np.arange(starts[s], starts[s] + new[s]) for s in keep]),
+                           device="cuda")
+    q2 = db.q[rows].contiguous()
+    n2 = [new[0], 0, new[2], new[3]]  # sequence 1 keeps its cached keys, loses its queries
+    k2 = [new[0], cached[1], cached[2] + new[2], new[3]]
+    cu_q2 = torch.as_tensor(np.concatenate([[0], np.cumsum(n2)]), dtype=torch.int32, device="cuda")
+    cu_k2 = torch.as_tensor(np.concatenate([[0], np.cumsum(k2)]), dtype=torch.int32, device="cuda")
+    out2 = torch.empty((len(rows), b.num_q_heads, b.head_dim), dtype=torch.bfloat16, device="cuda")
+    lib.paged_prefill_attn(out2, q2, db.k_cache, db.v_cache, db.block_tables, cu_q2, cu_k2,
+                           max(n2), b.scale, dev_status=db.status)
+    torch.cuda.synchronize()
+    assert db.status_value() == 0
+    assert torch.equal(out2, out[rows])
