@@ -736,8 +736,10 @@ __global__ void __launch_bounds__(kThreads)
 
 // Split-K merge: one CTA per (sequence, kv head) with more than one block.
 // M = max_b m_b;  O = sum_b 2^(m_b - M) o_b / sum_b 2^(m_b - M) l_b  (log2 units).
-// Threads are split into groups that take interleaved partials, so a long
-// context's partials are read in parallel; the groups are then summed in smem.
+// Threads are split into groups that take interleaved partials; each thread
+// merges its partials in one pass (running max, rescaling what it has so
+// far), so all of its loads are independent, and the groups are combined in
+// shared memory the same way.
 constexpr int kMergeThreads = 256;
 
 template <int D, int G>
@@ -747,7 +749,7 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
   constexpr int V4 = G * D / 4;  // float4 outputs per (sequence, kv head)
   constexpr int GR = V4 >= kMergeThreads ? 1 : kMergeThreads / V4;
   __shared__ float4 red[GR][V4];
-  __shared__ float sM[G], sInv[G];
+  __shared__ float sM[GR][G], sL[GR][G];
   const int Hkv = p.num_kv_heads;
   const int Hq = p.num_q_heads;
   const int s = blockIdx.x / Hkv;
@@ -758,60 +760,53 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
   if (pb0 < 0 || (int64_t)pb0 + nblk > p.max_total_blocks) return;  // never index past the workspace
   const int h0 = j * G;
   const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int lane = tid & 31;
-  for (int h = warp; h < G; h += kMergeThreads / 32) {
-    float M = -INFINITY;
-    for (int b = lane; b < nblk; b += 32)
-      M = fmaxf(M, __ldcg(p.part_ml + ((int64_t)(pb0 + b) * Hq + h0 + h) * 2));
-    M = warp_max(M);
-    float Ls = 0.f;
-    for (int b = lane; b < nblk; b += 32) {
-      const float *ml = p.part_ml + ((int64_t)(pb0 + b) * Hq + h0 + h) * 2;
-      Ls += fast_exp2(__ldcg(ml) - M) * __ldcg(ml + 1);
-    }
-    Ls = warp_sum(Ls);
-    if (lane == 0) {
-      sM[h] = M;
-      sInv[h] = 1.f / Ls;
-    }
-  }
-  __syncthreads();
   const int v = tid % V4;
   const int g = tid / V4;
   const int e = v * 4;
   const int h = e / D;
+  float M = -INFINITY, L = 0.f;
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
   if (g < GR) {
-    const float M = sM[h];
 #pragma unroll 4
     for (int b = g; b < nblk; b += GR) {
       const int64_t row = (int64_t)(pb0 + b) * Hq + h0 + h;
-      const float w = fast_exp2(__ldcg(p.part_ml + row * 2) - M);
+      const float2 ml = __ldcg(reinterpret_cast<const float2 *>(p.part_ml + row * 2));
       const float4 x = __ldcg(reinterpret_cast<const float4 *>(p.part_o + row * D + (e - h * D)));
-      o.x = fmaf(w, x.x, o.x);
-      o.y = fmaf(w, x.y, o.y);
-      o.z = fmaf(w, x.z, o.z);
-      o.w = fmaf(w, x.w, o.w);
+      const float Mn = fmaxf(M, ml.x);
+      const float a = fast_exp2(M - Mn);  // 0 while nothing is merged yet (M = -inf)
+      const float w = fast_exp2(ml.x - Mn);
+      o.x = fmaf(w, x.x, o.x * a);
+      o.y = fmaf(w, x.y, o.y * a);
+      o.z = fmaf(w, x.z, o.z * a);
+      o.w = fmaf(w, x.w, o.w * a);
+      L = fmaf(w, ml.y, L * a);
+      M = Mn;
     }
-    if (GR > 1) red[g][v] = o;
+    red[g][v] = o;
+    if (e - h * D == 0) {
+      sM[g][h] = M;
+      sL[g][h] = L;
+    }
   }
-  if (GR > 1) {
-    __syncthreads();
-    if (tid >= V4) return;
-    o = red[0][v];
+  __syncthreads();
+  if (tid >= V4) return;
+  // Combine the groups (a group without partials has M = -inf: factor 0).
+  float Mf = -INFINITY;
 #pragma unroll
-    for (int q = 1; q < GR; ++q) {
-      const float4 x = red[q][v];
-      o.x += x.x;
-      o.y += x.y;
-      o.z += x.z;
-      o.w += x.w;
-    }
-  } else if (tid >= V4) {
-    return;
+  for (int q = 0; q < GR; ++q) Mf = fmaxf(Mf, sM[q][h]);
+  float Lf = 0.f;
+  o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int q = 0; q < GR; ++q) {
+    const float c = fast_exp2(sM[q][h] - Mf);
+    const float4 x = red[q][v];
+    o.x = fmaf(c, x.x, o.x);
+    o.y = fmaf(c, x.y, o.y);
+    o.z = fmaf(c, x.z, o.z);
+    o.w = fmaf(c, x.w, o.w);
+    Lf = fmaf(c, sL[q][h], Lf);
   }
-  const float inv = sInv[h];
+  const float inv = 1.f / Lf;
   uint2 packed;
   packed.x = pack_bf16x2(o.x * inv, o.y * inv);
   packed.y = pack_bf16x2(o.z * inv, o.w * inv);
