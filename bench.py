@@ -366,8 +366,9 @@ def e2e_decode(pkv, b, dev, steps, warmup):
     the output back, as a serving loop would run it: the inputs of step i+1
     are copied (own stream) while step i computes, and the output of step i
     is read back (another stream) while step i+1 computes; device input and
-    output buffers alternate between two sets.  Returns (ms per step, H2D
-    bytes per step, D2H bytes per step)."""
+    output buffers alternate between two sets.  The timed loop replays a CUDA
+    graph of eight such steps.  Returns (ms per step, H2D bytes per step, D2H
+    bytes per step)."""
     import torch
 
     t = device_batch(b, dev, b.k_cache is None, b.seed)
@@ -402,14 +403,19 @@ def e2e_decode(pkv, b, dev, steps, warmup):
     computed = [torch.cuda.Event() for _ in range(2)]
     read = [torch.cuda.Event() for _ in range(2)]
 
-    def step(i):
+    def step(i, first_in_graph=False):
+        # (In a captured graph the first use of each buffer set waits for
+        # nothing: replays of the graph run one after another on the stream.)
         j = i % 2
+        reuse = not (first_in_graph and i < 2)
         with torch.cuda.stream(up):
-            up.wait_event(computed[j])  # the step that last used this input set is done
+            if reuse:
+                up.wait_event(computed[j])  # the step that last used this input set is done
             stage[j].copy_(host, non_blocking=True)
             copied[j].record(up)
         comp.wait_event(copied[j])
-        comp.wait_event(read[j])  # this output buffer's previous result was read back
+        if reuse:
+            comp.wait_event(read[j])  # this output buffer's previous result was read back
         x = ins[j]
         pkv.paged_decode_store_attn(out[j], x["q"], x["k"], x["v"], x["slot_mapping"],
                                     t["k_cache"], t["v_cache"], x["block_tables"],
@@ -423,18 +429,39 @@ def e2e_decode(pkv, b, dev, steps, warmup):
     for i in range(warmup):
         step(i)
     torch.cuda.synchronize()
+    # Eight steps (copies, kernels, read-backs and the streams' ordering) are
+    # captured once into a CUDA graph and replayed, as a serving loop replays
+    # its decode step: the host then issues one launch per eight steps
+    # instead of about ten calls per step.
+    per_graph = 8
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(comp)
+    with torch.cuda.stream(side):
+        cap = torch.cuda.current_stream()
+        comp = cap
+        with torch.cuda.graph(graph, stream=cap):
+            up.wait_stream(cap)
+            down.wait_stream(cap)
+            for i in range(per_graph):
+                step(i, first_in_graph=True)
+            cap.wait_stream(up)
+            cap.wait_stream(down)
+    comp = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    graph.replay()
+    torch.cuda.synchronize()
+    reps = max(1, steps // per_graph)
     s = torch.cuda.Event(enable_timing=True)
     e = torch.cuda.Event(enable_timing=True)
     s.record(comp)
-    for i in range(steps):
-        step(i)
-    for j in range(2):
-        comp.wait_event(read[j])  # the last results are back on the host
+    for _ in range(reps):
+        graph.replay()
     e.record(comp)
     torch.cuda.synchronize()
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item()):#x} in the end-to-end leg")
-    ms = s.elapsed_time(e) / steps
+    ms = s.elapsed_time(e) / (reps * per_graph)
     return ms, h2d, d2h
 
 
