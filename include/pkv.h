@@ -216,7 +216,10 @@ pkv_status pkv_paged_decode_attn_noalloc(uint16_t *out, const uint16_t *q,
  * memory, bf16 out.
  *
  * total_q = cu_seqlens_q[num_seqs]; max_seqlen_q bounds every n (a larger n
- * sets PKV_DEV_BAD_SEQLEN and its excess rows are not written).
+ * sets PKV_DEV_BAD_SEQLEN and its excess rows are not written).  A sequence
+ * with n = 0 has no rows.  A sequence's rows do not depend on the other
+ * sequences of the call or on their order (the kernel schedules the longest
+ * contexts first; the result is the same bit for bit).
  *
  * workspace: device memory of at least pkv_prefill_workspace_size() bytes,
  * 256-byte aligned, zero-filled before its first use.  It holds the counter
