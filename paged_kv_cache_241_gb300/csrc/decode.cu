@@ -818,24 +818,9 @@ pkv_status launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const Dec
                          int64_t max_items, cudaStream_t stream) {
   const DecodeSmem lay(D, G, prm.block_size, prm.num_seqs);
   const int smem = lay.total + 1024;  // + alignment slack
-  static int configured_smem = 0;
-  static int ctas_per_sm = 0;
-  if (configured_smem < smem) {
-    if (cudaFuncSetAttribute(paged_decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem) != cudaSuccess)
-      return PKV_ERR_CUDA;
-    configured_smem = smem;
-    ctas_per_sm = 0;
-  }
-  static int occ_smem = -1;
-  if (occ_smem != smem || ctas_per_sm == 0) {
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, paged_decode_kernel<D, G>, kThreads,
-                                                      smem) != cudaSuccess)
-      return PKV_ERR_CUDA;
-    ctas_per_sm = n > 0 ? n : 1;
-    occ_smem = smem;
-  }
+  int ctas_per_sm = 0;
+  if (!kernel_smem_setup((const void *)paged_decode_kernel<D, G>, kThreads, smem, &ctas_per_sm))
+    return PKV_ERR_CUDA;
   const int sms = device_sm_count();
   if (sms <= 0) return PKV_ERR_CUDA;
   int64_t grid = (int64_t)sms * ctas_per_sm;

@@ -1,7 +1,9 @@
 // host_common.cu -- status strings, device queries and tensor-map encoding.
 #include <cudaTypedefs.h>
 
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "host_common.h"
 
@@ -19,6 +21,36 @@ int device_sm_count() {
     cached[dev] = n;
   }
   return cached[dev];
+}
+
+bool kernel_smem_setup(const void *func, int threads, int bytes, int *ctas_per_sm) {
+  struct State {
+    int configured = 0;   // dynamic shared memory the kernel may use on this device
+    int occ_bytes = -1;   // bytes the occupancy below was computed for
+    int ctas = 0;
+  };
+  static std::mutex mu;
+  static std::map<std::pair<const void *, int>, State> states;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  State &st = states[std::make_pair(func, dev)];
+  if (st.configured < bytes) {
+    if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+        cudaSuccess)
+      return false;
+    st.configured = bytes;
+  }
+  if (st.occ_bytes != bytes) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, func, threads, (size_t)bytes) !=
+        cudaSuccess)
+      return false;
+    st.ctas = n > 0 ? n : 1;
+    st.occ_bytes = bytes;
+  }
+  *ctas_per_sm = st.ctas;
+  return true;
 }
 
 static PFN_cuTensorMapEncodeTiled_v12000 resolve_encode() {

@@ -12,6 +12,13 @@ namespace pkv {
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 
+// Let `func` (a __global__ function) use `bytes` of dynamic shared memory on
+// the current device (the attribute is per device; it is only ever raised)
+// and store in *ctas_per_sm how many of its CTAs of `threads` threads fit on
+// an SM with that much.  Cached per (kernel, device) and thread-safe.
+// Returns false on a CUDA error.
+bool kernel_smem_setup(const void *func, int threads, int bytes, int *ctas_per_sm);
+
 // Encode a bf16 tiled tensor map (driver entry point resolved at run time).
 // dims/strides follow cuTensorMapEncodeTiled: dims[0] is innermost, strides
 // are in bytes for dims 1..rank-1.  Returns false on failure.

@@ -781,22 +781,19 @@ template <int D, int NH>
 pkv_status launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                           const PrefillParams &prm, cudaStream_t stream) {
   using L = PrefillLayout<D, NH>;
-  static int smem = 0;
-  if (smem == 0) {
-    int bytes = L::total + 1024;
-    // Resident CTAs per SM must not ask for more than 512 TMEM columns in
-    // total, or tcgen05.alloc would stall: pad shared memory to cap occupancy.
-    const int max_ctas = 512 / L::kTmemCols;
-    const int per_sm = 228 * 1024;
-    const int min_bytes = per_sm / (max_ctas + 1) + 1;
-    if (bytes < min_bytes) bytes = min_bytes;
-    if (cudaFuncSetAttribute(paged_prefill_kernel<D, NH>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
-      return PKV_ERR_CUDA;
-    smem = bytes;
-  }
+  int smem = L::total + 1024;
+  // Resident CTAs per SM must not ask for more than 512 TMEM columns in
+  // total, or tcgen05.alloc would stall: pad shared memory to cap occupancy.
+  const int max_ctas = 512 / L::kTmemCols;
+  const int per_sm = 228 * 1024;
+  const int min_bytes = per_sm / (max_ctas + 1) + 1;
+  if (smem < min_bytes) smem = min_bytes;
+  int resident = 0;
+  if (!kernel_smem_setup((const void *)paged_prefill_kernel<D, NH>, threads_for<NH>(), smem,
+                         &resident))
+    return PKV_ERR_CUDA;
   // Persistent: as many CTAs as can be resident, no more than there are units.
-  const int ctas_per_sm = 512 / L::kTmemCols;
+  const int ctas_per_sm = resident < max_ctas ? resident : max_ctas;
   int64_t grid = (int64_t)device_sm_count() * ctas_per_sm;
   if (grid > (int64_t)prm.num_units) grid = prm.num_units;
   if (grid < 1) grid = 1;
