@@ -9,7 +9,8 @@
 //
 // Design (GB300): HBM-bound streaming, 16 bytes in and 64 bytes out per 32
 // weights.  A persistent grid (SMs x 8 CTAs of 256 threads) walks 32-weight
-// chunks: one 16-byte streaming load of four words, one scale, 32 products
+// chunks, four per thread per pass with their loads issued first: per chunk
+// one 16-byte streaming load of four words, one scale, 32 products
 // in bf16 pairs (u - 8 is exact in bf16; the multiply rounds the exact
 // product once to nearest even, as rounding an fp32 product would: that
 // product needs at most 12 significant bits), and two 32-byte (or four
@@ -73,30 +74,49 @@ __device__ __forceinline__ void dequant_word(uint32_t word, uint32_t scale2, uin
   out4[3] = prmt(r[2], r[3], 0x7632u);  // (w6, w7)
 }
 
+// U chunks per thread per pass, their loads issued before any arithmetic so
+// that more bytes are in flight per thread; I is the index type (32-bit when
+// every chunk index fits, which saves integer work per chunk).
+template <int U, typename I>
 __global__ void __launch_bounds__(kThreads)
     w4a16_dequant_kernel(uint16_t *__restrict__ out, const int32_t *__restrict__ packed,
-                         const uint16_t *__restrict__ scales, int64_t chunks,
-                         int64_t chunks_per_row, int64_t groups_per_row, int out_32b) {
-  const int64_t stride = (int64_t)gridDim.x * kThreads;
-  for (int64_t c = (int64_t)blockIdx.x * kThreads + threadIdx.x; c < chunks; c += stride) {
-    const int64_t row = c / chunks_per_row;
-    const int64_t cir = c - row * chunks_per_row;  // chunk in row: 32 weights
-    const uint4 w = ld_stream_u4(packed + c * 4);
-    const uint32_t sc = __ldg(scales + row * groups_per_row + cir / 4);
-    const uint32_t scale = sc | (sc << 16);  // the scale in both halves
-    uint32_t o[16];
-    dequant_word(w.x, scale, o);
-    dequant_word(w.y, scale, o + 4);
-    dequant_word(w.z, scale, o + 8);
-    dequant_word(w.w, scale, o + 12);
-    uint16_t *dst = out + c * 32;
-    if (out_32b) {
-      st_v8(dst, *reinterpret_cast<const uint32_t(*)[8]>(o));
-      st_v8(dst + 16, *reinterpret_cast<const uint32_t(*)[8]>(o + 8));
-    } else {
+                         const uint16_t *__restrict__ scales, int64_t chunks_,
+                         int64_t chunks_per_row_, int64_t groups_per_row_, int out_32b) {
+  const I chunks = (I)chunks_, cpr = (I)chunks_per_row_, gpr = (I)groups_per_row_;
+  const I stride = (I)gridDim.x * kThreads;
+  for (I c0 = (I)blockIdx.x * kThreads + threadIdx.x; c0 < chunks; c0 += stride * U) {
+    uint4 w[U];
+    uint32_t sc[U];
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        reinterpret_cast<uint4 *>(dst)[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+    for (int u = 0; u < U; ++u) {
+      const I c = c0 + (I)u * stride;
+      if (c < chunks) {
+        const I row = c / cpr;  // chunk in row: c - row * cpr, 32 weights each
+        w[u] = ld_stream_u4(packed + (int64_t)c * 4);
+        sc[u] = __ldg(scales + (int64_t)row * gpr + (c - row * cpr) / 4);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const I c = c0 + (I)u * stride;
+      if (c < chunks) {
+        const uint32_t scale = sc[u] | (sc[u] << 16);  // the scale in both halves
+        uint32_t o[16];
+        dequant_word(w[u].x, scale, o);
+        dequant_word(w[u].y, scale, o + 4);
+        dequant_word(w[u].z, scale, o + 8);
+        dequant_word(w[u].w, scale, o + 12);
+        uint16_t *dst = out + (int64_t)c * 32;
+        if (out_32b) {
+          st_v8(dst, *reinterpret_cast<const uint32_t(*)[8]>(o));
+          st_v8(dst + 16, *reinterpret_cast<const uint32_t(*)[8]>(o + 8));
+        } else {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            reinterpret_cast<uint4 *>(dst)[q] =
+                make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+        }
+      }
     }
   }
 }
@@ -122,7 +142,14 @@ extern "C" pkv_status pkv_w4a16_dequant(uint16_t *out, const int32_t *packed,
   const int64_t need = (chunks + kThreads - 1) / kThreads;
   if (grid > need) grid = need;
   const int out_32b = (reinterpret_cast<uintptr_t>(out) & 31u) == 0 ? 1 : 0;
-  w4a16_dequant_kernel<<<(unsigned)grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-      out, packed, scales, chunks, chunks_per_row, k / 128, out_32b);
+  constexpr int U = 4;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // 32-bit indices when no chunk index (plus a pass's stride) can overflow them.
+  if (chunks + grid * kThreads * U < ((int64_t)1 << 32))
+    w4a16_dequant_kernel<U, uint32_t><<<(unsigned)grid, kThreads, 0, st>>>(
+        out, packed, scales, chunks, chunks_per_row, k / 128, out_32b);
+  else
+    w4a16_dequant_kernel<U, int64_t><<<(unsigned)grid, kThreads, 0, st>>>(
+        out, packed, scales, chunks, chunks_per_row, k / 128, out_32b);
   return launch_status();
 }
