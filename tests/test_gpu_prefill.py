@@ -154,15 +154,16 @@ def test_prefill_output_only_16_byte_aligned(lib):
 
 
 @pytest.mark.parametrize("num_seqs", [256, 257])
-def test_prefill_many_sequences(lib, num_seqs):
+@pytest.mark.parametrize("D,G", [(128, 2), (64, 1)])
+def test_prefill_many_sequences(lib, num_seqs, D, G):
     # Up to 256 sequences the kernel orders them longest context first (sorted
     # in shared memory); beyond that it keeps their given order.  Both paths,
     # with many equal lengths (ties keep their index order) and one-token
-    # prompts.
+    # prompts, for two heads per CTA (D 128) and one (D 64).
     rng = np.random.default_rng(70 + num_seqs)
     new = [int(x) for x in rng.choice([1, 7, 40, 130], size=num_seqs)]
     cached = [int(x) for x in rng.choice([0, 0, 256, 300], size=num_seqs)]
-    b = wl.build_batch("many", "prefill", 70 + num_seqs, cached, new, 4, 2, 128)
+    b = wl.build_batch("many", "prefill", 70 + num_seqs + D, cached, new, 2 * G, 2, D)
     check_prefill(lib, b)
 
 
