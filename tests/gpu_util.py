@@ -1,5 +1,7 @@
 """Helpers for the GPU parity tests: move a workloads.PagedBatch to the device,
 run the library's calls on it, and compare with the oracle."""
+import os
+
 import numpy as np
 import torch
 
@@ -80,3 +82,69 @@ class DeviceBatch:
 
 def oracle_caches(b):
     return oracle.kv_store(b.k_cache, b.v_cache, b.k, b.v, b.slot_mapping)
+
+
+# ------------------------------------------- oracle over whole workloads, in parallel
+#
+# The full-size parity tests compare every output row.  The oracle is a plain
+# per-row loop, so its rows are computed in a pool of worker processes (spawn:
+# a forked child of a process that already holds a CUDA context can hang).
+# Each task is one sequence (or a slice of a long one's rows) passed to the
+# unchanged oracle as a batch of that one sequence.
+
+_POOL_STATE = {}
+
+
+def _pool_init(k_cache, v_cache, scale):
+    _POOL_STATE["kc"], _POOL_STATE["vc"], _POOL_STATE["scale"] = k_cache, v_cache, scale
+
+
+def _prefill_task(args):
+    q_seq, bt_row, n, len_k, r0, r1 = args
+    out = oracle.paged_prefill_attn(q_seq, _POOL_STATE["kc"], _POOL_STATE["vc"], bt_row[None, :],
+                                    np.array([0, n], np.int32), np.array([0, len_k], np.int32),
+                                    _POOL_STATE["scale"], rows=np.arange(r0, r1))
+    return out[r0:r1]
+
+
+_BLAS_VARS = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
+
+
+def _workers():
+    return max(1, min(16, os.cpu_count() or 1))
+
+
+def oracle_prefill_all_rows(b, ekc, evc, chunk=256):
+    """The oracle's output for every query row of prefill batch `b` (caches
+    `ekc`/`evc` after the store), float64 [T_q, Hq, D]."""
+    import multiprocessing as mp
+
+    cu_q, cu_k = b.cu_seqlens_q, b.cu_seqlens_k
+    tasks, where = [], []
+    for s in range(b.num_seqs):
+        q0, q1 = int(cu_q[s]), int(cu_q[s + 1])
+        n, len_k = q1 - q0, int(cu_k[s + 1] - cu_k[s])
+        for r0 in range(0, n, chunk):
+            r1 = min(n, r0 + chunk)
+            tasks.append((b.q[q0:q1], b.block_tables[s], n, len_k, r0, r1))
+            where.append((q0 + r0, q0 + r1))
+    out = np.full((b.q.shape[0], b.num_q_heads, b.head_dim), np.nan)
+    # the longest tasks (latest rows of the longest keys) first
+    order = sorted(range(len(tasks)), key=lambda i: -(tasks[i][3] - tasks[i][2] + tasks[i][5]))
+    ctx = mp.get_context("spawn")
+    # one BLAS thread per worker (the children read these when numpy loads)
+    saved = {v: os.environ.get(v) for v in _BLAS_VARS}
+    os.environ.update({v: "1" for v in _BLAS_VARS})
+    try:
+        with ctx.Pool(_workers(), initializer=_pool_init, initargs=(ekc, evc, b.scale)) as pool:
+            res = pool.map(_prefill_task, [tasks[i] for i in order], chunksize=1)
+    finally:
+        for v, x in saved.items():
+            if x is None:
+                os.environ.pop(v, None)
+            else:
+                os.environ[v] = x
+    for i, r in zip(order, res):
+        a, z = where[i]
+        out[a:z] = r
+    return out

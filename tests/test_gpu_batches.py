@@ -14,7 +14,8 @@ import torch
 
 import oracle
 import workloads as wl
-from gpu_util import DeviceBatch, assert_close, bf16, bits, i32, oracle_caches
+from gpu_util import (DeviceBatch, assert_close, bf16, bits, i32, oracle_caches,
+                      oracle_prefill_all_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -43,6 +44,19 @@ def test_mixed_decode_rows_and_prompt_chunks_in_one_prefill_launch(lib):
     assert db.status_value() == 0
     d = dec.double().cpu().numpy()
     assert np.all(np.abs(out.double().cpu().numpy()[rows] - d) <= 2 * (8e-3 + 1e-2 * np.abs(d)))
+
+
+def test_mixed_workload_full_size_every_row(lib):
+    # The benchmark's mixed step: 48 decode rows (contexts U[128, 2048]) and 8
+    # prompt chunks (U[256, 1024] new after U[0, 2048] cached) in one launch.
+    b = wl.mixed()
+    db = DeviceBatch(lib, b)
+    out = db.prefill()
+    assert db.status_value() == 0
+    ekc, evc = oracle_caches(b)
+    want = oracle_prefill_all_rows(b, ekc, evc)
+    assert not np.isnan(want).any()
+    assert_close(out.double().cpu().numpy(), want, "mixed step, every row")
 
 
 def shared_prefix_batch(kind, seed, cached, new):

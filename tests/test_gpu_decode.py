@@ -34,13 +34,9 @@ def test_decode_batch_full_size(lib):
     check_decode(lib, wl.decode())
 
 
-def test_longdecode_sampled_sequences(lib):
-    b = wl.longdecode()
-    L = b.context_lens
-    rng = np.random.default_rng(0)
-    seqs = sorted(set([int(np.argmax(L)), int(np.argmin(L))] +
-                      rng.choice(b.num_seqs, 30, replace=False).tolist()))
-    check_decode(lib, b, seqs=seqs)
+def test_longdecode_every_sequence(lib):
+    # 256 sequences, lognormal contexts up to 32768, 32 q / 8 kv heads
+    check_decode(lib, wl.longdecode())
 
 
 @pytest.mark.parametrize("D", [64, 128])

@@ -7,7 +7,7 @@ import torch
 
 import oracle
 import workloads as wl
-from gpu_util import DeviceBatch, assert_close, bits, oracle_caches
+from gpu_util import DeviceBatch, assert_close, bits, oracle_caches, oracle_prefill_all_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -26,13 +26,36 @@ def check_prefill(lib, b, rows=None):
 
 
 @pytest.mark.parametrize("D", [64, 128])
-@pytest.mark.parametrize("G", [1, 2, 4])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
 def test_prefill_varlen_with_prefix_small(lib, D, G):
     cached = [0, 256, 0, 512, 3, 0, 100]
     new = [1, 64, 127, 128, 129, 300, 200]
     b = wl.build_batch("small", "prefill", 50 + D + G, cached, new, 2 * G, 2, D,
                        max_blocks_pad=2)
     check_prefill(lib, b)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_prefill_single_row_units(lib, D, G):
+    # Units with one query row (decode rows of a mixed batch; the one-row tail
+    # of a 129- or 257-token prompt), contexts across the tile (64-key) and
+    # block (256-key) boundaries, with stale NaN in every slot past a context:
+    # one valid row in a 128-row MMA tile.
+    cached = [0, 15, 16, 17, 63, 64, 65, 255, 256, 257, 1000, 2047, 0, 300]
+    new = [1] * 12 + [129, 257]
+    b = wl.build_batch("rows1", "prefill", 80 + D + G, cached, new, 2 * G, 2, D, stale="nan")
+    db, out = check_prefill(lib, b)
+    assert torch.isfinite(out.float()).all()
+
+
+def test_prefill_single_row_of_context_one_returns_v_bits(lib):
+    b = wl.build_batch("one1", "prefill", 79, [0, 0, 0], [1, 1, 1], 8, 4, 128)
+    db = DeviceBatch(lib, b)
+    out = bits(db.prefill())
+    for s in range(3):
+        for h in range(8):
+            assert np.array_equal(out[s, h], b.v[s, h // 2])
 
 
 def test_prefill_single_tile_prompts_d128(lib):
@@ -93,16 +116,25 @@ def test_prefill_last_row_matches_decode(lib):
     assert np.all(np.abs(pre[last] - d) <= 2 * (8e-3 + 1e-2 * np.abs(d)))
 
 
-def test_prefill_full_size_sampled_rows(lib):
-    b = wl.prefill()
-    rows = wl.sample_rows(np.random.default_rng(1), b, per_seq=6)
-    check_prefill(lib, b, rows=rows)
+def check_every_row(lib, b):
+    """Every query row and head of a full-size workload against the oracle."""
+    db = DeviceBatch(lib, b)
+    out = db.prefill()
+    assert db.status_value() == 0
+    ekc, evc = oracle_caches(b)
+    want = oracle_prefill_all_rows(b, ekc, evc)
+    assert not np.isnan(want).any()
+    assert_close(out.double().cpu().numpy(), want, f"prefill {b.name}, every row")
 
 
-def test_prefix_cached_full_size_sampled_rows(lib):
-    b = wl.prefix()
-    rows = wl.sample_rows(np.random.default_rng(2), b, per_seq=6)
-    check_prefill(lib, b, rows=rows)
+def test_prefill_full_size_every_row(lib):
+    # 16 prompts, U[64, 4096] tokens (41K query rows), 16 q / 8 kv heads, D 128
+    check_every_row(lib, wl.prefill())
+
+
+def test_prefix_cached_full_size_every_row(lib):
+    # 32 sequences, k*256 cached (k in {0,1,2,4}) + U[1, 512] new tokens
+    check_every_row(lib, wl.prefix())
 
 
 def test_prefill_flags_inconsistent_seqlens(lib):

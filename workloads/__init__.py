@@ -272,22 +272,6 @@ WORKLOADS = {"tiny": tiny, "decode": decode, "longdecode": longdecode, "prefill"
              "prefix": prefix, "mixed": mixed}
 
 
-def sample_rows(rng: np.random.Generator, batch: PagedBatch, per_seq: int) -> np.ndarray:
-    """Sampled query-row indices for full-size checks: per sequence the first
-    and last row plus `per_seq` random rows in between."""
-    cu = batch.cu_seqlens_q
-    rows = []
-    for s in range(batch.num_seqs):
-        a, b = int(cu[s]), int(cu[s + 1])
-        if b <= a:
-            continue
-        pick = {a, b - 1}
-        if b - a > 2:
-            pick.update(rng.integers(a, b, size=min(per_seq, b - a)).tolist())
-        rows.extend(sorted(pick))
-    return np.asarray(rows, dtype=np.int64)
-
-
 # ------------------------------------------------ W4A16-G128 weight inputs
 
 @dataclass
