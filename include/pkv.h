@@ -102,7 +102,8 @@ pkv_status pkv_kv_store(const uint16_t *k, const uint16_t *v, uint16_t *k_cache,
 /*
  * Bytes of device workspace paged_decode_attn needs.  max_total_blocks is an
  * upper bound the caller guarantees on sum_s ceil(context_lens[s]/block_size)
- * (num_seqs * max_blocks_per_seq always works).
+ * (num_seqs * max_blocks_per_seq always works).  Returns 0 for invalid sizes
+ * and for sizes whose workspace would not fit a size_t.
  */
 size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                                  int64_t max_total_blocks);
@@ -127,7 +128,12 @@ size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads
  * share a workspace.
  *
  * Supported: head_dim in {64, 128}; Hq/Hkv in {1, 2, 4, 8}; block_size in
- * {64, 128, 256, 512}; num_seqs <= 16384.
+ * {64, 128, 256, 512}; num_seqs <= 16384, and the kernel's per-CTA shared
+ * memory (which holds every sequence's block offset and length) must fit in
+ * 227 KiB: only head_dim 128 with Hq/Hkv 8 and block_size 512 reaches that
+ * limit first, at 16107 sequences.  A batch beyond either limit returns
+ * PKV_ERR_UNSUPPORTED; sizes whose workspace cannot be addressed return
+ * PKV_ERR_INVALID_ARG.  Both launch nothing.
  */
 pkv_status pkv_paged_decode_attn(uint16_t *out, const uint16_t *q, const uint16_t *k_cache,
                                  const uint16_t *v_cache, const int32_t *block_tables,

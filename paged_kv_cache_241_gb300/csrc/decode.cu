@@ -45,6 +45,7 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;
 // that three CTAs still fit on an SM.
 __host__ __device__ constexpr int decode_stages(int G) { return G >= 4 ? 3 : 4; }
 constexpr int kMaxSeqs = 16384;
+constexpr int kMaxDynamicSmem = 232448;  // opt-in shared memory per CTA on sm_103 (227 KiB)
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct DecodeParams {
@@ -859,6 +860,12 @@ extern "C" size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int n
   if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
       max_total_blocks < 0)
     return 0;
+  // Sizes whose product would not fit a size_t (the factors are bounded first
+  // so that the per-block product itself cannot wrap) have no workspace.
+  if (num_q_heads > (1 << 16) || head_dim > (1 << 16)) return 0;
+  const size_t per_block = (size_t)num_q_heads * ((size_t)head_dim + 2) * 4;
+  if ((uint64_t)max_total_blocks > (SIZE_MAX / 2 - (size_t)num_seqs * 4 - 1024) / per_block)
+    return 0;
   return align256((size_t)(num_seqs + 1) * 4) +
          align256((size_t)max_total_blocks * num_q_heads * 2 * 4) +
          align256((size_t)max_total_blocks * num_q_heads * head_dim * 4);
@@ -893,8 +900,13 @@ pkv_status decode_call(uint16_t *out, const uint16_t *q, const uint16_t *k_cache
     return PKV_ERR_INVALID_ARG;
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
     return PKV_ERR_INVALID_ARG;
+  // The kernel keeps per-sequence block offsets and lengths in shared memory:
+  // batches whose layout would not fit are refused before any launch.
+  if (DecodeSmem(head_dim, G, block_size, num_seqs).total + 1024 > kMaxDynamicSmem)
+    return PKV_ERR_UNSUPPORTED;
   const size_t need =
       pkv_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_total_blocks);
+  if (need == 0) return PKV_ERR_INVALID_ARG;  // a workspace that size cannot be addressed
   if (workspace == nullptr || workspace_bytes < need ||
       (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return PKV_ERR_WORKSPACE;

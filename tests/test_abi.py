@@ -58,6 +58,9 @@ def test_workspace_size_formula(lib):
     assert lib.pkv_decode_workspace_size(S, Hq, Hkv, D, B) == \
         up((S + 1) * 4) + up(B * Hq * 2 * 4) + up(B * Hq * D * 4)
     assert lib.pkv_decode_workspace_size(0, Hq, Hkv, D, B) == 0
+    # a block bound whose workspace would wrap a size_t has no workspace size
+    assert lib.pkv_decode_workspace_size(S, Hq, Hkv, D, 1 << 62) == 0
+    assert lib.pkv_decode_workspace_size(S, 1 << 20, Hkv, D, B) == 0
 
 
 NULL = None
@@ -103,6 +106,15 @@ def test_decode_rejects_bad_arguments(lib):
     assert decode_call(lib, out=p, q=p, kc=p, vc=p, bt=p, cl=p, ws=ctypes.c_void_p(0x10010),
                        wsb=need) == 3
     assert decode_call(lib, S=0) == 0                     # empty batch
+    # a workspace bound too large to address: rejected before anything runs
+    assert decode_call(lib, out=p, q=p, kc=p, vc=p, bt=p, cl=p, ws=p, wsb=1 << 40,
+                       mtb=1 << 62) == 1
+    # the shared-memory layout of the largest group and block size holds at
+    # most 16107 sequences; other shapes reach the 16384-sequence limit first
+    big = dict(out=p, q=p, kc=p, vc=p, bt=p, cl=p, Hq=64, Hkv=8, BS=512)
+    assert decode_call(lib, **big, S=16108) == 2
+    assert decode_call(lib, **big, S=16107) == 3          # fits: the (missing) workspace is next
+    assert decode_call(lib, out=p, q=p, kc=p, vc=p, bt=p, cl=p, S=16384) == 3
 
 
 def prefill_call(lib, **kw):
