@@ -20,7 +20,8 @@ the path) on this host on a bounded sample of the same workload.
 """
 import os
 
-# The CPU oracle is timed single-threaded: pin BLAS/OpenMP before numpy loads.
+# The CPU oracle runs one BLAS thread per worker process (the workers are
+# spawned and read these when numpy loads).
 for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
     os.environ.setdefault(_v, "1")
 
@@ -360,18 +361,22 @@ class Arm:
         return total, attn_ms, store_ms
 
 
-def e2e_decode(pkv, b, dev, steps, warmup):
+def e2e_decode(pkv, b, dev, steps, warmup, copies=4):
     """Decode step through host buffers: every step copies the step's inputs
     from pinned host memory (one packed copy), stores + attends, and copies
     the output back, as a serving loop would run it: the inputs of step i+1
     are copied (own stream) while step i computes, and the output of step i
     is read back (another stream) while step i+1 computes; device input and
-    output buffers alternate between two sets.  The timed loop replays a CUDA
-    graph of eight such steps.  Returns (ms per step, H2D bytes per step, D2H
+    output buffers alternate between two sets, and the caches rotate over
+    `copies` copies.  The timed loop replays a CUDA graph of eight such steps.  Returns (ms per step, H2D bytes per step, D2H
     bytes per step)."""
     import torch
 
     t = device_batch(b, dev, b.k_cache is None, b.seed)
+    # The caches rotate over `copies` copies, as in the kernel leg, so no step
+    # finds the previous step's K/V in L2.
+    caches = [(t["k_cache"], t["v_cache"])] + [(t["k_cache"].clone(), t["v_cache"].clone())
+                                               for _ in range(copies - 1)]
     names = ("q", "k", "v", "slot_mapping", "block_tables", "context_lens")
     offs, nbytes = {}, 0
     for k in names:  # packed layout, every input 256-byte aligned
@@ -417,8 +422,9 @@ def e2e_decode(pkv, b, dev, steps, warmup):
         if reuse:
             comp.wait_event(read[j])  # this output buffer's previous result was read back
         x = ins[j]
+        kc, vc = caches[i % copies]
         pkv.paged_decode_store_attn(out[j], x["q"], x["k"], x["v"], x["slot_mapping"],
-                                    t["k_cache"], t["v_cache"], x["block_tables"],
+                                    kc, vc, x["block_tables"],
                                     x["context_lens"], b.scale, ws[j], mtb, status)
         computed[j].record(comp)
         with torch.cuda.stream(down):
@@ -466,32 +472,143 @@ def e2e_decode(pkv, b, dev, steps, warmup):
 
 
 # ------------------------------------------------------------ oracle timing
+#
+# The CPU baseline is the fp64 oracle as it stands, run on this host's cores:
+# the work of a step (the decode batch's sequences, or a sample of a prefill
+# batch's query rows) is spread over a pool of worker processes, one BLAS
+# thread each.  The pool is started with `spawn` (a process forked after CUDA
+# was initialised can hang), and the caches live in shared memory, so the
+# workers attach to them instead of receiving copies.
 
-def oracle_decode_timing(b, budget_s=8.0):
-    """Time the fp64 CPU oracle on whole decode steps of batch b (single thread)."""
+_ORACLE = {}
+
+
+def _oracle_worker_init(names, shapes, scale):
+    from multiprocessing import shared_memory
+
+    segs = [shared_memory.SharedMemory(name=n) for n in names]
+    _ORACLE["segs"] = segs  # keeps the mappings alive
+    _ORACLE["kc"] = np.ndarray(shapes[0], dtype=np.uint16, buffer=segs[0].buf)
+    _ORACLE["vc"] = np.ndarray(shapes[1], dtype=np.uint16, buffer=segs[1].buf)
+    _ORACLE["scale"] = scale
+
+
+def _oracle_decode_task(args):
     import oracle
 
-    kc, vc = b.k_cache, b.v_cache
-    passes = 0
-    t0 = time.perf_counter()
-    while True:
-        kc2, vc2 = oracle.kv_store(kc, vc, b.k, b.v, b.slot_mapping)
-        oracle.paged_decode_attn(b.q, kc2, vc2, b.block_tables, b.context_lens, b.scale)
-        passes += 1
-        el = time.perf_counter() - t0
-        if el >= budget_s or passes >= 50:
-            break
-    return el / passes, passes
+    q, bt_row, L = args
+    return oracle.paged_decode_attn(q, _ORACLE["kc"], _ORACLE["vc"], bt_row[None, :],
+                                    np.array([L], np.int32), _ORACLE["scale"])
 
 
-def oracle_sample_batch():
-    """Bounded sample of the decode workload for the CPU oracle: the first 16
-    of its 64 sequences (cache materialised on the host)."""
+def _oracle_prefill_task(args):
+    import oracle
+
+    q_seq, bt_row, n, len_k, rows = args
+    return oracle.paged_prefill_attn(q_seq, _ORACLE["kc"], _ORACLE["vc"], bt_row[None, :],
+                                     np.array([0, n], np.int32), np.array([0, len_k], np.int32),
+                                     _ORACLE["scale"], rows=rows)
+
+
+class OraclePool:
+    """Worker processes that run the oracle over one batch's caches (which
+    have already been through the oracle's kv_store)."""
+
+    def __init__(self, b, kc, vc, workers=None):
+        import multiprocessing as mp
+        from multiprocessing import shared_memory
+
+        self.workers = workers or max(1, os.cpu_count() or 1)
+        self.segs = []
+        names, shapes = [], []
+        for a in (kc, vc):
+            seg = shared_memory.SharedMemory(create=True, size=max(1, a.nbytes))
+            np.ndarray(a.shape, dtype=np.uint16, buffer=seg.buf)[...] = a
+            self.segs.append(seg)
+            names.append(seg.name)
+            shapes.append(a.shape)
+        self.pool = mp.get_context("spawn").Pool(self.workers, initializer=_oracle_worker_init,
+                                                 initargs=(names, shapes, b.scale))
+        self.pool.map(abs, range(self.workers))  # every worker up before any timing
+
+    def map(self, fn, tasks):
+        return self.pool.map(fn, tasks, chunksize=1)
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+        for seg in self.segs:
+            seg.close()
+            seg.unlink()
+
+
+def oracle_decode_batch():
+    """The decode workload (64 sequences, contexts U[128, 2048], 16 q / 8 kv
+    heads, D 128) with its cache materialised on the host in a pool sized to
+    the contexts (the full workload's 1024-block pool differs only in unused
+    blocks)."""
     full = wl.decode(fill_cache=False)
-    n = 16
-    return wl.build_batch("decode-sample", "decode", 2, full.cached_lens[:n], full.new_lens[:n],
+    return wl.build_batch("decode", "decode", 2, full.cached_lens, full.new_lens,
                           full.num_q_heads, full.num_kv_heads, full.head_dim,
-                          num_blocks=sum(wl.blocks_for(L) for L in full.context_lens[:n]))
+                          num_blocks=full.total_blocks_used)
+
+
+def oracle_decode_steps(steps, warmup=1, batch=None):
+    """Seconds per decode step of the oracle on all host cores: its kv_store of
+    the step's 64 new tokens (one call), then its attention for every sequence
+    (a pool task per sequence, longest first).  Returns (s/step, batch, workers)."""
+    import oracle
+
+    b = batch or oracle_decode_batch()
+    kc, vc = oracle.kv_store(b.k_cache, b.v_cache, b.k, b.v, b.slot_mapping)
+    pool = OraclePool(b, kc, vc)
+    order = np.argsort(-b.context_lens, kind="stable")
+    tasks = [(b.q[s:s + 1], b.block_tables[s], int(b.context_lens[s])) for s in order]
+    times = []
+    try:
+        for i in range(warmup + steps):
+            t0 = time.perf_counter()
+            oracle.kv_store(b.k_cache, b.v_cache, b.k, b.v, b.slot_mapping)
+            pool.map(_oracle_decode_task, tasks)
+            if i >= warmup:
+                times.append(time.perf_counter() - t0)
+    finally:
+        pool.close()
+    return sum(times) / len(times), b, pool.workers
+
+
+def oracle_prefill_sample(stride=32):
+    """TFLOP/s of the oracle on all host cores over a sample of the varlen
+    prefill workload (16 prompts, U[64, 4096] tokens, 16 q / 8 kv heads,
+    D 128): every `stride`-th query row of every prompt and its last row,
+    each sequence's sampled rows one pool task.  Flops count the sampled rows'
+    unmasked keys, as for the kernel.  Returns a cpu_baseline record."""
+    import oracle
+
+    b = wl.prefill()
+    kc, vc = oracle.kv_store(b.k_cache, b.v_cache, b.k, b.v, b.slot_mapping)
+    cu_q, cu_k = b.cu_seqlens_q, b.cu_seqlens_k
+    tasks, pairs, nrows = [], 0, 0
+    for s in range(b.num_seqs):
+        q0, q1 = int(cu_q[s]), int(cu_q[s + 1])
+        n, len_k = q1 - q0, int(cu_k[s + 1] - cu_k[s])
+        rows = np.unique(np.concatenate([np.arange(0, n, stride), [n - 1]]))
+        pairs += int(np.sum(len_k - n + rows + 1))
+        nrows += len(rows)
+        tasks.append((b.q[q0:q1], b.block_tables[s], n, len_k, rows))
+    tasks.sort(key=lambda t: -int(np.sum(t[3] - t[2] + t[4] + 1)))
+    pool = OraclePool(b, kc, vc)
+    try:
+        t0 = time.perf_counter()
+        pool.map(_oracle_prefill_task, tasks)
+        el = time.perf_counter() - t0
+    finally:
+        pool.close()
+    flops = 4 * b.head_dim * b.num_q_heads * pairs
+    return {"value": flops / el / 1e12, "unit": "TFLOP/s", "cores": pool.workers,
+            "kind": "oracle", "seconds": el,
+            "sample": f"prefill: one query row in {stride} and the last row of each of the 16 "
+                      f"prompts ({nrows} of {b.q.shape[0]} rows, all 16 heads)"}
 
 
 # ------------------------------------------------------------ main
@@ -502,37 +619,34 @@ def dist_env():
 
 
 def run_reference(args):
+    """The reference arm: the fp64 oracle on this host's cores, timed on the
+    decode workload (every step the whole 64-sequence batch), plus its
+    prefill throughput on a row sample."""
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    import oracle
-
-    b = oracle_sample_batch()
-    times = []
-    for i in range(args.warmup + args.steps):
-        t0 = time.perf_counter()
-        kc, vc = oracle.kv_store(b.k_cache, b.v_cache, b.k, b.v, b.slot_mapping)
-        oracle.paged_decode_attn(b.q, kc, vc, b.block_tables, b.context_lens, b.scale)
-        if i >= args.warmup:
-            times.append(time.perf_counter() - t0)
-    per = sum(times) / len(times)
+    per, b, workers = oracle_decode_steps(args.steps, warmup=min(args.warmup, 2))
     gbs = (decode_bytes(b) + store_bytes(b)) / per / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": per * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": "decode: 16 of the 64 sequences of the decode batch "
-                               "(contexts U[128,2048], 16 q / 8 kv heads, D=128, block 256)",
+        "config": {"workload": "decode: 64 seqs, contexts U[128,2048], 16 q / 8 kv heads, D=128, "
+                               "block 256; per step the 64 new tokens' K/V are stored and decode "
+                               "attention runs",
                    "l2": "n/a (CPU)"},
-        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": "16 of 64 decode sequences per step"},
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": workers, "kind": "oracle",
+                         "sample": "the whole decode batch every step (kv_store in one process, "
+                                   "attention one sequence per worker task)"},
         "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "prefill": {"cpu_baseline": oracle_prefill_sample()},
     }
     print(json.dumps(line))
     return 0
 
-DEFAULT_COPIES = {"decode": 4, "longdecode": 3, "prefill": 4, "prefix": 8}
+
+DEFAULT_COPIES = {"decode": 4, "longdecode": 3, "prefill": 4, "prefix": 8, "mixed": 8}
 MAKERS = {"decode": wl.decode, "longdecode": wl.longdecode, "prefill": wl.prefill,
           "prefix": wl.prefix, "mixed": wl.mixed}
 
@@ -639,6 +753,8 @@ def main():
             else:
                 tf = prefill_flops(bb) / (am * 1e-3) / 1e12
                 rec["tflops"] = tf
+                # context: each sequence's K/V read once, plus q and out
+                rec["hbm_gbs_kv_once"] = prefill_bytes(bb) / (am * 1e-3) / 1e9
                 rec["roofline"] = {"bound": "tensor", "achieved": tf,
                                    "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                                    "frac": tf / peaks["bf16_tflops"],
@@ -697,12 +813,14 @@ def main():
     }
     line.update(extra)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        sb = oracle_sample_batch()
-        per, passes = oracle_decode_timing(sb)
+        steps = 20
+        per, sb, workers = oracle_decode_steps(steps)
         line["cpu_baseline"] = {"value": (decode_bytes(sb) + store_bytes(sb)) / per / 1e9,
-                                "unit": "GB/s", "cores": 1, "kind": "oracle",
-                                "sample": f"16 of the 64 decode sequences, {passes} passes, "
-                                          f"{per:.2f} s per pass"}
+                                "unit": "GB/s", "cores": workers, "kind": "oracle",
+                                "sample": f"the whole 64-sequence decode batch, {steps} steps, "
+                                          f"{per:.3f} s per step"}
+        if "prefill" in line:
+            line["prefill"]["cpu_baseline"] = oracle_prefill_sample()
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
