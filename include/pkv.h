@@ -209,6 +209,22 @@ pkv_status pkv_paged_decode_attn_noalloc(uint16_t *out, const uint16_t *q,
                                          float scale, int32_t *dev_status, void *stream);
 
 /*
+ * test_decode_fault -- TEST-ONLY fault injection for the decode kernels'
+ * bounded waits (the pages have no counterpart; it exists so that tests can
+ * make a wait run out without faulting or hanging the GPU).
+ *
+ * Sets, for the current device, the wall-clock limit of every wait in the
+ * decode kernels (default 1 s) and a tile number that every decode CTA's
+ * producer then skips instead of loading (-1: none, the default).  A decode
+ * call made while a tile is withheld waits out the limit, flags
+ * PKV_DEV_TIMEOUT in *dev_status, leaves its output undefined and returns;
+ * the device stays usable.  Restore with pkv_test_decode_fault(1000000000, -1).
+ * Synchronous (it copies to device memory).  Returns PKV_ERR_INVALID_ARG for
+ * wait_limit_ns <= 0 or withhold_tile < -1.
+ */
+pkv_status pkv_test_decode_fault(int64_t wait_limit_ns, int withhold_tile);
+
+/*
  * paged_prefill_attn -- causal attention of packed variable-length prompts
  * over the paged cache, including an already-cached prefix.
  *

@@ -53,6 +53,7 @@ SIGNATURES = {
                                         _c_int, _c_int, _c_int, _c_int, _c_int, _c_i64, _c_f, _p,
                                         _c_sz, _p, _p]),
     "pkv_prefill_workspace_size": (_c_sz, []),
+    "pkv_test_decode_fault": (_c_int, [_c_i64, _c_int]),
     "pkv_w4a16_dequant": (_c_int, [_p, _p, _p, _c_i64, _c_i64, _c_int, _p]),
     "pkv_bm_create": (_p, [_c_int, _c_int]),
     "pkv_bm_destroy": (None, [_p]),
@@ -234,6 +235,15 @@ def paged_decode_attn_noalloc(out, q, k_cache, v_cache, block_tables, context_le
         _ptr(context_lens), S, Hq, Hkv, D, BS, block_tables.shape[1], NB, int(max_total_blocks),
         float(scale), _ptr(dev_status), _stream(stream))
     _check(st, "pkv_paged_decode_attn_noalloc")
+
+
+def test_decode_fault(wait_limit_ns: int, withhold_tile: int) -> None:
+    """TEST ONLY: shorten the decode kernels' wait limit on the current device
+    and make every decode CTA skip loading its tile number `withhold_tile`
+    (-1: none), so that a decode call times out and reports PKV_DEV_TIMEOUT.
+    Restore with test_decode_fault(10**9, -1)."""
+    _check(load().pkv_test_decode_fault(int(wait_limit_ns), int(withhold_tile)),
+           "test_decode_fault")
 
 
 def prefill_workspace(device="cuda"):

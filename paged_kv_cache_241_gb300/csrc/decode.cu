@@ -45,6 +45,12 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;
 // that three CTAs still fit on an SM.
 __host__ __device__ constexpr int decode_stages(int G) { return G >= 4 ? 3 : 4; }
 constexpr int kMaxSeqs = 16384;
+
+// Test-only fault injection, set by pkv_test_decode_fault: the producer of
+// every CTA skips the tile it would issue as its number `withhold` (counting
+// from 0; -1 = none), so that tile's consumers wait until the wait limit runs
+// out.  Read once per CTA.
+static __device__ int g_decode_withhold_tile = -1;
 constexpr int kMaxDynamicSmem = 232448;  // opt-in shared memory per CTA on sm_103 (227 KiB)
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -359,6 +365,7 @@ __global__ void __launch_bounds__(kThreads)
   // 3-deep ring: lane 0 alone issues the q copy and every tile by TMA.
   if (!slot_by_lanes<kStages>(1) && warp == kConsumerWarps) {
     if (lane == 0) {
+      const int withhold = g_decode_withhold_tile;
       const uint64_t policy = l2_policy_evict_first();
       int issued = 0;
       int item_no = 0;
@@ -402,9 +409,11 @@ __global__ void __launch_bounds__(kThreads)
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(&full[st], kTileBytes);
-            tma_load_4d_hint(tiles + st * kTileBytes, map, &full[st], 0, j, t * kTile, blk,
-                             policy);
+            if (issued != withhold) {
+              mbar_arrive_expect_tx(&full[st], kTileBytes);
+              tma_load_4d_hint(tiles + st * kTileBytes, map, &full[st], 0, j, t * kTile, blk,
+                               policy);
+            }
             ++issued;
           }
         }
@@ -425,6 +434,7 @@ __global__ void __launch_bounds__(kThreads)
     constexpr int kChunks = D / 8;       // 16-byte chunks per token row
     constexpr int kRowsPer = 32 / kChunks;  // token rows per warp-wide copy
     const uint64_t policy = l2_policy_evict_first();
+    const int withhold = g_decode_withhold_tile;
     const int part = lane % kChunks;
     const int row0 = lane / kChunks;
     int issued = 0;
@@ -475,7 +485,9 @@ __global__ void __launch_bounds__(kThreads)
             ok = __shfl_sync(0xffffffffu, good ? 1 : 0, 0) != 0;
             if (!ok) break;
           }
-          if (slot_by_lanes<kStages>(st)) {
+          if (issued == withhold) {
+            // (test-only: nothing issued, the slot's consumers time out)
+          } else if (slot_by_lanes<kStages>(st)) {
             // Token rows t*64 .. t*64+63 of block blk, kv head j: row r is
             // (blk*BS + t*64 + r)*Hkv + j rows of D into the cache.
             const uint16_t *src =
@@ -1077,4 +1089,18 @@ extern "C" pkv_status pkv_paged_decode_attn_noalloc(
                                num_q_heads, num_kv_heads, head_dim, block_size,
                                max_blocks_per_seq, num_blocks, max_total_blocks, scale, scratch,
                                kNoAllocScratchBytes, dev_status, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Test-only fault injection for the bounded waits of the decode kernel.
+// ---------------------------------------------------------------------------
+
+extern "C" pkv_status pkv_test_decode_fault(int64_t wait_limit_ns, int withhold_tile) {
+  if (wait_limit_ns <= 0 || withhold_tile < -1) return PKV_ERR_INVALID_ARG;
+  const unsigned long long limit = (unsigned long long)wait_limit_ns;
+  if (cudaMemcpyToSymbol(pkv::g_wait_limit_ns, &limit, sizeof(limit)) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  if (cudaMemcpyToSymbol(pkv::g_decode_withhold_tile, &withhold_tile, sizeof(int)) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  return PKV_OK;
 }

@@ -18,6 +18,10 @@ namespace pkv {
 // microseconds; one second means the pipeline is broken.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
+// The limit the waits use.  Each translation unit has its own copy, fixed at
+// kWaitLimitNs except where a test hook shortens it (decode only).
+static __device__ unsigned long long g_wait_limit_ns = kWaitLimitNs;
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -78,7 +82,7 @@ static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parit
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 15u) == 0) {
       if (abort != nullptr && *abort) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (global_timer_ns() - t0 > g_wait_limit_ns) {
         if (abort != nullptr) *abort = 1;
         return false;
       }

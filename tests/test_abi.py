@@ -143,6 +143,12 @@ def test_prefill_rejects_bad_arguments(lib):
     assert prefill_call(lib, **ptrs, ws=ctypes.c_void_p(0x10010), wsb=need) == 3
 
 
+def test_decode_fault_hook_rejects_bad_arguments(lib):
+    # checked before any device call
+    assert lib.pkv_test_decode_fault(0, -1) == 1
+    assert lib.pkv_test_decode_fault(1000, -2) == 1
+
+
 def test_dequant_rejects_bad_arguments(lib):
     f = lib.pkv_w4a16_dequant
     p = ctypes.c_void_p(0x10000)
