@@ -163,24 +163,40 @@ def job_throughput(total_ms, steps, units_per_step, world, device="cpu"):
 
 # ------------------------------------------------------------ ncu counters
 
-def ncu_traffic(kernel):
-    """DRAM bytes per launch (read + write) of `kernel` from the committed ncu
-    summary, or None when there is none or the kernel's sources changed since
-    the counters were taken (source hash recorded beside them)."""
+def ncu_traffic(*kernels):
+    """DRAM bytes per call (read + write, summed over the call's kernels) from
+    the committed ncu summary (profiles/counters.json, keyed by kernel, with
+    "@workload" when one kernel is recorded on several workloads), or None
+    when a record is missing or its kernel's sources changed since the
+    counters were taken (source hash recorded beside them)."""
     import hashlib
 
     try:
         with open(os.path.join(ROOT, "profiles", "counters.json")) as f:
-            rec = json.load(f)[kernel]
-        h = hashlib.sha256()
-        for src in rec["sources"]:
-            with open(os.path.join(ROOT, "paged_kv_cache_241_gb300", src), "rb") as g:
-                h.update(g.read())
-        if h.hexdigest()[:16] != rec["source_sha256_16"]:
-            return None
-        return int(rec["dram_read_bytes"]) + int(rec["dram_write_bytes"])
+            recs = json.load(f)
+        total = 0
+        for kernel in kernels:
+            rec = recs[kernel]
+            h = hashlib.sha256()
+            for src in rec["sources"]:
+                with open(os.path.join(ROOT, "paged_kv_cache_241_gb300", src), "rb") as g:
+                    h.update(g.read())
+            if h.hexdigest()[:16] != rec["source_sha256_16"]:
+                return None
+            total += int(rec["dram_read_bytes"]) + int(rec["dram_write_bytes"])
+        return total
     except Exception:
         return None
+
+
+# The counters records of each workload's call (see profiles/counters.json).
+TRAFFIC_KEYS = {
+    "decode": ("paged_decode_kernel<128,2>", "decode_merge_kernel<128,2>"),
+    "longdecode": ("paged_decode_kernel<128,4>@longdecode", "decode_merge_kernel<128,4>@longdecode"),
+    "prefill": ("paged_prefill_kernel<128,2>",),
+    "prefix": ("paged_prefill_kernel<128,2>@prefix",),
+    "mixed": ("paged_prefill_kernel<128,2>@mixed",),
+}
 
 
 # ------------------------------------------------------------ clock sampling
@@ -749,7 +765,9 @@ def main():
             if bb.kind == "decode":
                 ach = decode_bytes(bb) / (am * 1e-3) / 1e9
                 rec["roofline"] = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"],
-                                   "unit": "GB/s", "frac": ach / peaks["hbm_gbs"]}
+                                   "unit": "GB/s", "frac": ach / peaks["hbm_gbs"],
+                                   "traffic": ncu_traffic(*TRAFFIC_KEYS[name]),
+                                   "bytes_per_launch": decode_bytes(bb)}
             else:
                 tf = prefill_flops(bb) / (am * 1e-3) / 1e12
                 rec["tflops"] = tf
@@ -758,8 +776,8 @@ def main():
                 rec["roofline"] = {"bound": "tensor", "achieved": tf,
                                    "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                                    "frac": tf / peaks["bf16_tflops"],
-                                   "traffic": ncu_traffic("paged_prefill_kernel<128,2>")
-                                   if name == "prefill" else None}
+                                   "traffic": ncu_traffic(*TRAFFIC_KEYS[name]),
+                                   "flops_per_launch": prefill_flops(bb)}
                 kvb = store_bytes(bb) / (sm_ * 1e-3) / 1e9
                 rec["kv_store"] = {"GB/s": kvb, "frac": kvb / peaks["hbm_gbs"],
                                    "bytes": store_bytes(bb)}
@@ -799,7 +817,7 @@ def main():
                    "step_bytes": step_bytes},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                     "traffic": ncu_traffic("paged_decode_kernel<128,2>"),
+                     "traffic": ncu_traffic(*TRAFFIC_KEYS["decode"]),
                      "kernel": ("paged_decode_kernel<128,2> (kv_store fused) + decode_merge_kernel"
                                 "<128,2>" if fused else
                                 "paged_decode_kernel<128,2> + decode_merge_kernel<128,2>"),
