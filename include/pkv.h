@@ -100,9 +100,10 @@ pkv_status pkv_kv_store(const uint16_t *k, const uint16_t *v, uint16_t *k_cache,
                         int32_t *dev_status, void *stream);
 
 /*
- * Bytes of device workspace paged_decode_attn needs.  max_total_blocks is an
- * upper bound the caller guarantees on sum_s ceil(context_lens[s]/block_size)
- * (num_seqs * max_blocks_per_seq always works).  Returns 0 for invalid sizes
+ * Bytes of device workspace paged_decode_attn needs: a 256-byte work counter,
+ * then the split-K scratch.  max_total_blocks is an upper bound the caller
+ * guarantees on sum_s ceil(context_lens[s]/block_size) (num_seqs *
+ * max_blocks_per_seq always works).  Returns 0 for invalid sizes
  * and for sizes whose workspace would not fit a size_t.
  */
 size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
@@ -117,21 +118,24 @@ size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads
  * g = Hq / Hkv.  bf16 in, fp32 accumulation, bf16 out (round to nearest even).
  *
  * Split-K flash-decoding: each (sequence, kv head, block) is one work item
- * whose partial (max, sum, unnormalised output) goes to the workspace; a
- * second kernel, launched as a programmatic dependent of the first, merges
- * the partials of every sequence that spans more than one block.  Two kernel
- * launches per call (one when max_blocks_per_seq == 1).
+ * whose partial (max, sum, unnormalised output) goes to the workspace; the
+ * persistent CTAs take items from a counter in the workspace as they become
+ * free.  A second kernel, launched as a programmatic dependent of the first,
+ * merges the partials of every sequence that spans more than one block.  Two
+ * kernel launches per call (one when max_blocks_per_seq == 1).
  *
  * workspace: device buffer of at least pkv_decode_workspace_size(...) bytes,
- * 256-byte aligned.  Its contents need no initialisation: every call writes
- * each entry before reading it.  Calls that overlap on the device must not
+ * 256-byte aligned, zero-filled once before its first use.  Its first 256
+ * bytes hold the work counter, which every call leaves at zero (also a call
+ * whose waits ran out); the rest needs no initialisation (each call writes
+ * every entry before reading it).  Calls that overlap on the device must not
  * share a workspace.
  *
  * Supported: head_dim in {64, 128}; Hq/Hkv in {1, 2, 4, 8}; block_size in
  * {64, 128, 256, 512}; num_seqs <= 16384, and the kernel's per-CTA shared
  * memory (which holds every sequence's block offset and length) must fit in
  * 227 KiB: only head_dim 128 with Hq/Hkv 8 and block_size 512 reaches that
- * limit first, at 16107 sequences.  A batch beyond either limit returns
+ * limit first, at 16097 sequences.  A batch beyond either limit returns
  * PKV_ERR_UNSUPPORTED; sizes whose workspace cannot be addressed return
  * PKV_ERR_INVALID_ARG.  Both launch nothing.
  */
@@ -191,9 +195,10 @@ pkv_status pkv_paged_decode_store_attn(uint16_t *out, const uint16_t *q, const u
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
  * before any stream capture.  Each call then runs the same kernels as
- * pkv_paged_decode_attn on that array; the array keeps the previous call's
- * contents, but nothing in it needs to start at zero (each call writes every
- * entry before reading it).  All calls on a device share the one array, so
+ * pkv_paged_decode_attn on that array.  The array is zero when the library
+ * loads and keeps the previous call's contents: its work counter (the first
+ * 256 bytes) is left at zero by every call, and the rest is written before it
+ * is read.  All calls on a device share the one array, so
  * calls that overlap on the GPU (other streams, other host threads) race and
  * corrupt each other's results: serialise them.
  *

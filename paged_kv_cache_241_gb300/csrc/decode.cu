@@ -8,10 +8,15 @@
 // nano-vllm hub page, "core tech 4").
 //
 // Design (GB300):
-//  * Work item = (sequence, kv head, logical block).  Items are equal-sized
-//    (one block of K and V for one head), so a persistent grid of
-//    (#SM x resident CTAs) walks them round-robin with no host sync; every CTA
-//    derives the item list itself from context_lens (block-wide scan in smem).
+//  * Work item = (sequence, kv head, logical block).  A persistent grid of
+//    (#SM x resident CTAs) walks the items with no host sync: every CTA
+//    derives the item list from context_lens itself (block-wide scan in
+//    smem).  With many items per CTA they are handed out by an atomic counter
+//    in the caller's workspace, each CTA taking the next one when its producer
+//    is ready for it, so the CTAs finish together although items and SMs
+//    differ in speed; with few, round-robin (the counter's round trip then
+//    costs more than the balance gains).  The last CTA to finish leaves the
+//    counter zeroed for the next call.
 //  * One producer warp streams the item's K tiles, then its V tiles, as 4-D
 //    TMA boxes {D, 1 head, 64 tokens, 1 block} into a ring of shared-memory
 //    stages; the block-table lookup is the box's outer coordinate.  With a
@@ -45,6 +50,11 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;
 // that three CTAs still fit on an SM.
 __host__ __device__ constexpr int decode_stages(int G) { return G >= 4 ? 3 : 4; }
 constexpr int kMaxSeqs = 16384;
+constexpr int kItemSlots = 4;       // depth of the shared ring of fetched item indices
+// Items per CTA from which they are handed out by the counter instead of
+// round-robin: measured, long skewed decode (33 per CTA) 365 -> 351 us with
+// the counter, the 64-sequence decode batch (6 per CTA) 60.1 -> 61.2 us.
+constexpr int kCounterRounds = 12;
 
 // Test-only fault injection, set by pkv_test_decode_fault: the producer of
 // every CTA skips the tile it would issue as its number `withhold` (counting
@@ -56,6 +66,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 struct DecodeParams {
   uint16_t *out;
+  unsigned int *ctl;    // [0]: next item to hand out, [1]: CTAs done (both 0 between calls)
   const uint16_t *q;
   const int32_t *block_tables;
   const int32_t *context_lens;
@@ -213,17 +224,19 @@ __device__ __forceinline__ void load_prob_pairs(const float2 *p, float2 (&pv)[G]
 
 // Shared-memory carve-up (bytes), shared by host and device.
 struct DecodeSmem {
-  int tiles, qbuf, bars, logits, red, stats, misc, prefix, ctx, total;
+  int tiles, qbuf, bars, logits, red, stats, misc, iring, prefix, ctx, total;
   __host__ __device__ DecodeSmem(int D, int G, int bs, int num_seqs) {
     tiles = 0;
     const int stages = decode_stages(G);
     qbuf = tiles + stages * kTile * D * 2;  // [2][G*D] bf16: q of the next items
-    bars = qbuf + 2 * G * D * 2;            // full[S], empty[S], q_full[2], q_empty[2]
-    logits = bars + (2 * stages + 4) * 8;   // [block_size][G] float pairs
+    // full[S], empty[S], q_full[2], q_empty[2], item_full[R], item_empty[R]
+    bars = qbuf + 2 * G * D * 2;
+    logits = bars + (2 * stages + 4 + 2 * kItemSlots) * 8;  // [block_size][G] float pairs
     red = logits + ((bs * G * 8 + 15) & ~15);
     stats = red + kConsumerWarps * G * D * 4;
     misc = stats + 2 * G * 4;
-    prefix = misc + 16;
+    iring = misc + 16;                      // [R] fetched item indices
+    prefix = iring + kItemSlots * 4;
     ctx = prefix + (num_seqs + 1) * 4;
     total = ctx + num_seqs * 4;
   }
@@ -260,6 +273,9 @@ __global__ void __launch_bounds__(kThreads)
   uint64_t *empty = full + kStages;
   uint64_t *q_full = empty + kStages;
   uint64_t *q_empty = q_full + 2;
+  uint64_t *item_full = q_empty + 2;        // [kItemSlots]: an item index is in the ring
+  uint64_t *item_empty = item_full + kItemSlots;
+  volatile int *iring = reinterpret_cast<volatile int *>(smem + lay.iring);
   // Per token and head: phase 1 stores the logit in .x, phase 2 replaces the
   // pair by (p, p) so phase 3 can feed it straight to a packed FMA.
   float2 *logits = reinterpret_cast<float2 *>(smem + lay.logits);  // [block_size][G]
@@ -289,6 +305,10 @@ __global__ void __launch_bounds__(kThreads)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&q_full[i], 1);
       mbar_init(&q_empty[i], kConsumerWarps);
+    }
+    for (int i = 0; i < kItemSlots; ++i) {
+      mbar_init(&item_full[i], 1);
+      mbar_init(&item_empty[i], kConsumerWarps);
     }
     misc[0] = 0;
     fence_barrier_init();
@@ -361,6 +381,35 @@ __global__ void __launch_bounds__(kThreads)
     b = gblk - prefix[s];
   };
 
+  // Producer side of the item ring (lane 0 of the producer warp): the next
+  // item index (from the shared counter, or round-robin), and its hand-over
+  // to the consumers (an index >= total_items tells them to stop).
+  const bool by_counter = total_items >= kCounterRounds * (int)gridDim.x;
+  int round_no = 0;
+  auto fetch_item = [&]() -> int {
+    if (!by_counter) return (int)blockIdx.x + (round_no++) * (int)gridDim.x;
+    return (int)atomicAdd(&p.ctl[0], 1u);
+  };
+  auto publish_item = [&](int item_no, int w) -> bool {
+    const int slot = item_no % kItemSlots;
+    if (item_no >= kItemSlots &&
+        !mbar_wait_bounded(&item_empty[slot], ((item_no / kItemSlots) - 1) & 1, abort_flag))
+      return false;
+    iring[slot] = w;
+    mbar_arrive(&item_full[slot]);  // (release: orders the store above)
+    return true;
+  };
+  // Every CTA's producer calls this once on its way out: the last one resets
+  // the counters for the next call on this workspace.
+  auto leave = [&]() {
+    __threadfence();
+    if (atomicAdd(&p.ctl[1], 1u) == gridDim.x - 1) {
+      p.ctl[0] = 0;
+      p.ctl[1] = 0;
+      __threadfence();
+    }
+  };
+
   // ---- producer warp: q, then K tiles, then V tiles of every item ----------
   // 3-deep ring: lane 0 alone issues the q copy and every tile by TMA.
   if (!slot_by_lanes<kStages>(1) && warp == kConsumerWarps) {
@@ -371,20 +420,21 @@ __global__ void __launch_bounds__(kThreads)
       int item_no = 0;
       bool ok = true;
       int s, b, j, gblk;
+      int w = fetch_item();
       int blk_next = 0;
-      if (blockIdx.x < total_items) {
-        item_coords(blockIdx.x, s, b, j, gblk);
+      if (w < total_items) {
+        item_coords(w, s, b, j, gblk);
         blk_next = p.block_tables[(int64_t)s * p.max_blocks_per_seq + b];
       }
-      for (int w = blockIdx.x; w < total_items && ok; w += gridDim.x, ++item_no) {
+      for (;; ++item_no) {
+        if (!publish_item(item_no, w)) {
+          ok = false;
+          break;
+        }
+        if (w >= total_items) break;
+        const int wn = fetch_item();  // the next item (its value is first needed below)
         item_coords(w, s, b, j, gblk);
         int blk = blk_next;
-        const int wn = w + gridDim.x;
-        if (wn < total_items) {  // fetch the next item's block id early
-          int sn, bn, jn, gn;
-          item_coords(wn, sn, bn, jn, gn);
-          blk_next = p.block_tables[(int64_t)sn * p.max_blocks_per_seq + bn];
-        }
         if (blk < 0 || (int64_t)blk >= p.num_blocks) {
           flag_status(p.status, PKV_DEV_BAD_BLOCK);
           blk = 0;
@@ -417,6 +467,16 @@ __global__ void __launch_bounds__(kThreads)
             ++issued;
           }
         }
+        if (!ok) {
+          ++item_no;  // this item's q copy was issued: the drain below waits for it
+          break;
+        }
+        w = wn;
+        if (w < total_items) {  // the next item's block id, read early
+          int sn, bn, jn, gn;
+          item_coords(w, sn, bn, jn, gn);
+          blk_next = p.block_tables[(int64_t)sn * p.max_blocks_per_seq + bn];
+        }
       }
       if (!ok) flag_status(p.status, PKV_DEV_TIMEOUT);
       // Do not leave while copies into this CTA's shared memory are in flight.
@@ -424,6 +484,7 @@ __global__ void __launch_bounds__(kThreads)
         if (!mbar_wait_bounded(&full[i % kStages], (i / kStages) & 1, nullptr)) flag_status(p.status, PKV_DEV_TIMEOUT);
       for (int i = max(0, item_no - 2); i < item_no; ++i)
         if (!mbar_wait_bounded(&q_full[i & 1], (i >> 1) & 1, nullptr)) flag_status(p.status, PKV_DEV_TIMEOUT);
+      leave();
     }
     return;
   }
@@ -442,19 +503,22 @@ __global__ void __launch_bounds__(kThreads)
     bool ok = true;
     int s, b, j, gblk;
     int blk_next = 0;
-    if (blockIdx.x < total_items) {
-      item_coords(blockIdx.x, s, b, j, gblk);
+    int w = lane == 0 ? fetch_item() : 0;
+    w = __shfl_sync(0xffffffffu, w, 0);
+    if (w < total_items) {
+      item_coords(w, s, b, j, gblk);
       blk_next = p.block_tables[(int64_t)s * p.max_blocks_per_seq + b];
     }
-    for (int w = blockIdx.x; w < total_items && ok; w += gridDim.x, ++item_no) {
+    for (;; ++item_no) {
+      {
+        const bool good = lane == 0 ? publish_item(item_no, w) : true;
+        ok = __shfl_sync(0xffffffffu, good ? 1 : 0, 0) != 0;
+        if (!ok) break;
+      }
+      if (w >= total_items) break;
+      const int wn_lane0 = lane == 0 ? fetch_item() : 0;  // the next item, first needed below
       item_coords(w, s, b, j, gblk);
       int blk = blk_next;
-      const int wn = w + gridDim.x;
-      if (wn < total_items) {  // fetch the next item's block id early
-        int sn, bn, jn, gn;
-        item_coords(wn, sn, bn, jn, gn);
-        blk_next = p.block_tables[(int64_t)sn * p.max_blocks_per_seq + bn];
-      }
       if (blk < 0 || (int64_t)blk >= p.num_blocks) {
         if (lane == 0) flag_status(p.status, PKV_DEV_BAD_BLOCK);
         blk = 0;
@@ -506,7 +570,18 @@ __global__ void __launch_bounds__(kThreads)
           ++issued;
         }
       }
+      if (!ok) {
+        ++item_no;  // this item's q copy was issued: the drain below waits for it
+        break;
+      }
+      w = __shfl_sync(0xffffffffu, wn_lane0, 0);
+      if (w < total_items) {  // the next item's block id, read early
+        int sn, bn, jn, gn;
+        item_coords(w, sn, bn, jn, gn);
+        blk_next = p.block_tables[(int64_t)sn * p.max_blocks_per_seq + bn];
+      }
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");
     if (lane == 0) {
       if (!ok) flag_status(p.status, PKV_DEV_TIMEOUT);
       // Do not leave while copies into this CTA's shared memory are in flight.
@@ -516,8 +591,8 @@ __global__ void __launch_bounds__(kThreads)
       for (int i = max(0, item_no - 2); i < item_no; ++i)
         if (!mbar_wait_bounded(&q_full[i & 1], (i >> 1) & 1, nullptr))
           flag_status(p.status, PKV_DEV_TIMEOUT);
+      leave();
     }
-    asm volatile("cp.async.wait_all;" ::: "memory");
     return;
   }
 
@@ -525,8 +600,22 @@ __global__ void __launch_bounds__(kThreads)
   const int r = lane & 7;     // lane within its octet
   const int gid = lane >> 3;  // octet index: 4 tokens each
   int ctile = 0;              // tiles consumed so far
-  int item_no = 0;
-  for (int w = blockIdx.x; w < total_items; w += gridDim.x, ++item_no) {
+  for (int item_no = 0;; ++item_no) {
+    // The next item index from the producer's ring; the four warps decide
+    // together whether to go on (a wait that ran out stops all of them).
+    int w = total_items;
+    {
+      const int slot = item_no % kItemSlots;
+      const bool got =
+          mbar_wait_bounded(&item_full[slot], (item_no / kItemSlots) & 1, abort_flag);
+      if (got) w = iring[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&item_empty[slot]);
+      if (named_bar_or(1, kConsumerWarps * 32, (!got || w >= total_items) ? 1 : 0)) {
+        if (!got && tid == 0) flag_status(p.status, PKV_DEV_TIMEOUT);
+        break;
+      }
+    }
     int s, b, j, gblk;
     item_coords(w, s, b, j, gblk);
     const int valid = min(BS, ctx[s] - b * BS);
@@ -878,7 +967,7 @@ extern "C" size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int n
   const size_t per_block = (size_t)num_q_heads * ((size_t)head_dim + 2) * 4;
   if ((uint64_t)max_total_blocks > (SIZE_MAX / 2 - (size_t)num_seqs * 4 - 1024) / per_block)
     return 0;
-  return align256((size_t)(num_seqs + 1) * 4) +
+  return 256 /* item counter */ + align256((size_t)(num_seqs + 1) * 4) +
          align256((size_t)max_total_blocks * num_q_heads * 2 * 4) +
          align256((size_t)max_total_blocks * num_q_heads * head_dim * 4);
 }
@@ -929,6 +1018,8 @@ pkv_status decode_call(uint16_t *out, const uint16_t *q, const uint16_t *k_cache
   prm.block_tables = block_tables;
   prm.context_lens = context_lens;
   uint8_t *ws = static_cast<uint8_t *>(workspace);
+  prm.ctl = reinterpret_cast<unsigned int *>(ws);
+  ws += 256;
   prm.seq_prefix = reinterpret_cast<int32_t *>(ws);
   ws += align256((size_t)(num_seqs + 1) * 4);
   prm.part_ml = reinterpret_cast<float *>(ws);
@@ -1083,8 +1174,9 @@ extern "C" pkv_status pkv_paged_decode_attn_noalloc(
   void *scratch = nullptr;
   const pkv_status st = scratch_for_current_device(&scratch);
   if (st != PKV_OK) return st;
-  // The array keeps the previous call's contents; nothing in it has to start
-  // at zero: every call writes each entry it later reads.
+  // The array keeps the previous call's contents.  Its work counter (first
+  // 256 bytes) starts at zero when the library loads and every call leaves
+  // it at zero; the rest is written by each call before it is read.
   return pkv_paged_decode_attn(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
                                num_q_heads, num_kv_heads, head_dim, block_size,
                                max_blocks_per_seq, num_blocks, max_total_blocks, scale, scratch,

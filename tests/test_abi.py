@@ -51,12 +51,13 @@ def test_status_strings(lib):
 
 
 def test_workspace_size_formula(lib):
-    # sequence prefix ((S+1) int32) + partial max/sum (B*Hq*2 f32) + partial outputs
-    # (B*Hq*D f32), each rounded up to 256 bytes
+    # work counter (256 bytes) + sequence prefix ((S+1) int32) + partial
+    # max/sum (B*Hq*2 f32) + partial outputs (B*Hq*D f32), each rounded up to
+    # 256 bytes
     up = lambda x: (x + 255) // 256 * 256
     S, Hq, Hkv, D, B = 64, 16, 8, 128, 300
     assert lib.pkv_decode_workspace_size(S, Hq, Hkv, D, B) == \
-        up((S + 1) * 4) + up(B * Hq * 2 * 4) + up(B * Hq * D * 4)
+        256 + up((S + 1) * 4) + up(B * Hq * 2 * 4) + up(B * Hq * D * 4)
     assert lib.pkv_decode_workspace_size(0, Hq, Hkv, D, B) == 0
     # a block bound whose workspace would wrap a size_t has no workspace size
     assert lib.pkv_decode_workspace_size(S, Hq, Hkv, D, 1 << 62) == 0
@@ -110,10 +111,10 @@ def test_decode_rejects_bad_arguments(lib):
     assert decode_call(lib, out=p, q=p, kc=p, vc=p, bt=p, cl=p, ws=p, wsb=1 << 40,
                        mtb=1 << 62) == 1
     # the shared-memory layout of the largest group and block size holds at
-    # most 16107 sequences; other shapes reach the 16384-sequence limit first
+    # most 16097 sequences; other shapes reach the 16384-sequence limit first
     big = dict(out=p, q=p, kc=p, vc=p, bt=p, cl=p, Hq=64, Hkv=8, BS=512)
-    assert decode_call(lib, **big, S=16108) == 2
-    assert decode_call(lib, **big, S=16107) == 3          # fits: the (missing) workspace is next
+    assert decode_call(lib, **big, S=16098) == 2
+    assert decode_call(lib, **big, S=16097) == 3          # fits: the (missing) workspace is next
     assert decode_call(lib, out=p, q=p, kc=p, vc=p, bt=p, cl=p, S=16384) == 3
 
 

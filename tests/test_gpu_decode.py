@@ -39,6 +39,31 @@ def test_longdecode_every_sequence(lib):
     check_decode(lib, wl.longdecode())
 
 
+def counter_batch(G, seed):
+    """Many items per CTA (about 14K (sequence, kv head, 64-token block)
+    items): the kernel then hands items out through its workspace counter."""
+    rng = np.random.default_rng(seed)
+    L = rng.integers(3000, 4000, size=128, endpoint=True)
+    return wl.build_batch("counter", "decode", seed, L - 1, np.ones(128, np.int64), 2 * G, 2, 64,
+                          block_size=64, rng=rng)
+
+
+@pytest.mark.parametrize("G", [2, 4])  # 4-deep ring (TMA + cp.async), 3-deep ring (TMA)
+def test_decode_items_handed_out_by_the_counter(lib, G):
+    b = counter_batch(G, 49 + G)
+    db, out = check_decode(lib, b)
+
+
+def test_decode_batch_of_4096_sequences(lib):
+    # A large batch: every CTA keeps all 4096 sequences' block offsets and
+    # lengths in shared memory, and the items are handed out by the counter.
+    rng = np.random.default_rng(48)
+    L = rng.integers(1, 200, size=4096, endpoint=True)
+    b = wl.build_batch("big", "decode", 48, L - 1, np.ones(4096, np.int64), 4, 2, 128,
+                       block_size=64, rng=rng)
+    check_decode(lib, b)
+
+
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("G", [1, 2, 4, 8])
 def test_decode_edge_lengths(lib, D, G):
@@ -89,20 +114,26 @@ def test_decode_workspace_reuse_gives_identical_results(lib):
     assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])
 
 
-def test_decode_workspace_needs_no_initialisation(lib):
+def test_decode_workspace_needs_only_its_counter_zeroed(lib):
+    # The first 256 bytes (the work counter) must start at zero and every call
+    # leaves them at zero; the split-K scratch after them needs no
+    # initialisation.
     b = wl.build_batch("dirty", "decode", 45, [700, 2000, 40, 5000], [1, 1, 1, 1], 16, 8, 128)
     db = DeviceBatch(lib, b)
     mtb = b.total_blocks_used
     clean = lib.decode_workspace(b.num_seqs, 16, 8, 128, mtb)
-    dirty = torch.full_like(clean, 0xFF)  # every byte 0xFF: NaN floats, -1 ints
+    dirty = torch.full_like(clean, 0xFF)  # scratch bytes 0xFF: NaN floats, -1 ints
+    dirty[:256] = 0
     outs = []
-    for ws in (clean, dirty):
+    for ws in (clean, dirty, dirty):
         out = torch.empty((b.num_seqs, 16, 128), dtype=torch.bfloat16, device="cuda")
         lib.paged_decode_attn(out, db.q, db.k_cache, db.v_cache, db.block_tables,
                               db.context_lens, b.scale, ws, mtb, db.status)
         outs.append(bits(out))
+        torch.cuda.synchronize()
+        assert int(ws[:256].count_nonzero().item()) == 0
     assert db.status_value() == 0
-    assert np.array_equal(outs[0], outs[1])
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
 
 
 def test_decode_flags_bad_context_block_and_workspace(lib):

@@ -17,10 +17,25 @@ from gpu_util import DeviceBatch, assert_close, oracle_caches
 pytestmark = pytest.mark.gpu
 
 
+def few_items(G):
+    # fewer items than CTAs: items taken round-robin
+    return wl.build_batch("limit", "decode", 90 + G, [4, 299, 700], [1, 1, 1], 2 * G, 2, 64,
+                          num_blocks=12)
+
+
+def many_items(G):
+    # ~14K items: handed out by the workspace counter, which must be left at
+    # zero even by a call whose waits ran out
+    rng = np.random.default_rng(95 + G)
+    L = rng.integers(3000, 4000, size=128, endpoint=True)
+    return wl.build_batch("limit", "decode", 95 + G, L - 1, np.ones(128, np.int64), 2 * G, 2, 64,
+                          block_size=64, rng=rng)
+
+
+@pytest.mark.parametrize("make", [few_items, many_items])
 @pytest.mark.parametrize("G", [2, 4])  # 4-stage ring (TMA + cp.async) and 3-stage ring (TMA)
-def test_decode_wait_runs_out_then_next_call_is_correct(lib, G):
-    b = wl.build_batch("limit", "decode", 90 + G, [4, 299, 700], [1, 1, 1], 2 * G, 2, 64,
-                       num_blocks=12)
+def test_decode_wait_runs_out_then_next_call_is_correct(lib, G, make):
+    b = make(G)
     db = DeviceBatch(lib, b)
     mtb = b.total_blocks_used
     ws = lib.decode_workspace(b.num_seqs, b.num_q_heads, b.num_kv_heads, b.head_dim, mtb)
@@ -33,6 +48,7 @@ def test_decode_wait_runs_out_then_next_call_is_correct(lib, G):
     finally:
         lib.test_decode_fault(1_000_000_000, -1)
     assert db.status_value() & lib.DEV_TIMEOUT
+    assert int(ws[:256].count_nonzero().item()) == 0  # the work counter is left at zero
     db.status.zero_()
     lib.paged_decode_attn(out, db.q, db.k_cache, db.v_cache, db.block_tables, db.context_lens,
                           b.scale, ws, mtb, db.status)
