@@ -668,7 +668,17 @@ MAKERS = {"decode": wl.decode, "longdecode": wl.longdecode, "prefill": wl.prefil
 
 
 def run_single(args, pkv, dev, peaks, peak_src):
-    """One workload alone: `steps` timed steps of store + attention."""
+    """One workload alone: `steps` timed steps of store + attention (or of
+    the W4A16-G128 dequantisation)."""
+    if args.workload == "dequant":
+        w = wl.dequant()
+        ms = time_dequant(pkv, w, dev, args.steps, args.warmup, copies=args.copies or 4)
+        gbs = dequant_bytes(w) / (ms * 1e-3) / 1e9
+        print(json.dumps({"workload": "dequant", "steps": args.steps, "warmup": args.warmup,
+                          "kernel_ms": ms, "metric": "dequant GB/s", "value": gbs, "unit": "GB/s",
+                          "frac": gbs / peaks["hbm_gbs"], "bytes": dequant_bytes(w),
+                          "peak_source": peak_src}))
+        return 0
     b = MAKERS[args.workload](fill_cache=False)
     arm = Arm(pkv, b, dev, copies=args.copies or DEFAULT_COPIES[args.workload],
               fused=False if args.separate_store else None)
@@ -699,7 +709,7 @@ def main():
     ap.add_argument("--only-main", action="store_true",
                     help="headline decode step only (no other workloads)")
     ap.add_argument("--workload", default="all",
-                    choices=["all", "decode", "longdecode", "prefill", "prefix", "mixed"],
+                    choices=["all", "decode", "longdecode", "prefill", "prefix", "mixed", "dequant"],
                     help="run one workload alone (small runs for profiling)")
     ap.add_argument("--separate-store", action="store_true",
                     help="decode: time kv_store and decode as two calls instead of the fused call")
