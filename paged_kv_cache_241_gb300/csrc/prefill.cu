@@ -45,6 +45,8 @@ constexpr int BM = 128;  // query rows per tile (MMA M)
 constexpr int BN = 64;   // keys per tile
 constexpr int kUnitSlots = 4;  // depth of the shared ring of fetched units
 constexpr int kMaxSorted = 256;  // sequences ordered longest-first in shared memory (more: as given)
+constexpr int kPackMaxQ = 1024;  // longest prompt (new tokens) for which the packing kernel runs
+constexpr int kPackMeanQ = 128;  // largest mean new tokens per sequence for it
 // Warp 0: unit fetcher + Q/K TMA producer; warp 1: S = QK^T MMA issuer;
 // warp 2: V TMA producer; warp 3: P.V MMA issuer; then one 4-warp softmax
 // group per head.
@@ -91,13 +93,14 @@ __device__ __forceinline__ void st_global_v8(void *ptr, const uint32_t (&w)[8]) 
 // h_first .. h_first + NH - 1, keys [0, n_kv * BN) of the sequence.
 struct Unit {
   int s, q_begin, len_k, c, q0, rows_valid, n_kv, h_first, kvh;
+  int pack;  // both heads' rows in one 128-row tile (rows_valid <= 64; packing kernels only)
 };
 
 // Unit index -> unit (sequence-major, heaviest tile of a sequence first, head
 // groups innermost; sequences longest context first when `order` is in use).
 // False when the index has no work (a tile past a short prompt) or its
 // lengths are inconsistent (then PKV_DEV_BAD_SEQLEN is set).
-template <int NH>
+template <int NH, bool kPack>
 __device__ bool decode_unit(unsigned int idx, const PrefillParams &p, const uint32_t *order,
                             Unit &u) {
   const int HG = p.num_q_heads / NH;
@@ -129,6 +132,7 @@ __device__ bool decode_unit(unsigned int idx, const PrefillParams &p, const uint
   u.n_kv = (min(len_k, c + u.q0 + u.rows_valid) + BN - 1) / BN;  // keys the tile needs
   u.h_first = hg * NH;
   u.kvh = u.h_first / (p.num_q_heads / p.num_kv_heads);
+  u.pack = (kPack && NH == 2 && u.rows_valid <= BM / 2) ? 1 : 0;
   return true;
 }
 
@@ -259,9 +263,10 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
 
 // Barrier phases below count tiles (g) and units (iu) over the CTA's whole
 // run, so they carry across unit boundaries.
-template <int D, int NH>
+template <int D, int NH, bool kPack>
 __global__ void __launch_bounds__(threads_for<NH>(), 1)
     paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
+                         const __grid_constant__ CUtensorMap tm_q64,
                          const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
   using L = PrefillLayout<D, NH>;
@@ -367,6 +372,7 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
     bool ok = true;
     if (is_k && lane == 0) {
       tma_prefetch_map(&tm_q);
+      if (kPack) tma_prefetch_map(&tm_q64);
       tma_prefetch_map(&tm_k);
     } else if (lane == 0) {
       tma_prefetch_map(&tm_v);
@@ -387,7 +393,7 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
           for (;;) {
             const unsigned int i = atomicAdd(&p.ws->next_unit, 1u);
             if (i >= p.num_units) break;
-            if (decode_unit<NH>(i, p, order, u)) {
+            if (decode_unit<NH, kPack>(i, p, order, u)) {
               have = true;
               break;
             }
@@ -414,7 +420,16 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
         if (is_k) {
           // Q of this unit once the previous unit's S MMAs are done with Q.
           if (iu >= 2) ok = mbar_wait_bounded(q_empty, (iu - 2) & 1, abort_flag);
-          if (ok) {
+          if (ok && kPack && u.pack) {
+            // Packed unit: each head's first 64 query rows, head h in rows
+            // 64h .. 64h + 63 of the first head's Q tile.
+            ++q_loads;
+            mbar_arrive_expect_tx(q_full, NH * L::kQBytes / 2);
+            for (int h = 0; h < NH; ++h)
+              for (int x = 0; x < XR; ++x)
+                tma_load_3d(sQ + x * BM * 128 + h * (BM / 2) * 128, &tm_q64, q_full, x * 64,
+                            u.h_first + h, u.q_begin + u.q0);
+          } else if (ok) {
             ++q_loads;
             mbar_arrive_expect_tx(q_full, NH * L::kQBytes);
             for (int h = 0; h < NH; ++h)
@@ -472,6 +487,9 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
     // descriptors are built once; an MMA only adds the operand's offset to
     // the address field (bits 0-13, bytes / 16).
     int iu = 0, g = 0;
+    // Packing kernels: head 1 takes no part in packed units, so its S/P
+    // buffers and O count their own tiles (g1) and units (u1).
+    int g1 = 0, u1 = 0;
     bool ok = true;
     Unit u;
     if (warp == kSWarp) {
@@ -479,18 +497,22 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
       const uint64_t dq = umma_desc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t dk = umma_desc_sw128(smem_u32(sK), 16, 1024);
       while (ok && next_unit(iu, u)) {
+        const bool pk = kPack && u.pack;
         if (lane == 0) {
           ok = mbar_wait_bounded(q_full, (iu - 1) & 1, abort_flag);
           // Per tile: S_h for every head into buffer g & 1 once K is in
           // and the P.V two tiles back (which read P from that buffer) is done.
+          // A packed unit has one 128-row S (both heads' rows) in head 0's buffers.
           for (int jt = 0; jt < u.n_kv && ok; ++jt, ++g) {
             const int st = g % kKStages;
             ok = mbar_wait_bounded(&k_full[st], (g / kKStages) & 1, abort_flag);
             const uint64_t dk_st = dk + (uint64_t)((st * L::kKVBytes) >> 4);
-            const int b = g & 1;
 #pragma unroll
             for (int h = 0; h < NH && ok; ++h) {
-              if (g >= 2) ok = mbar_wait_bounded(&p_free[2 * h + b], ((g - 2) >> 1) & 1, abort_flag);
+              if (pk && h > 0) break;
+              const int gh = (kPack && h == 1) ? g1 + jt : g;  // head h's tile count
+              const int b = gh & 1;
+              if (gh >= 2) ok = mbar_wait_bounded(&p_free[2 * h + b], ((gh - 2) >> 1) & 1, abort_flag);
               if (!ok) break;
               tc_fence_after_sync();
               const uint32_t d = tmem + kSCol + (2 * h + b) * BN;
@@ -509,42 +531,52 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
         }
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         g = __shfl_sync(0xffffffffu, g, 0);
+        if (kPack && !pk) g1 += u.n_kv;
       }
     } else {
       constexpr uint32_t idesc_o = umma_idesc_bf16(BM, D, false, true);
       const uint64_t dv = umma_desc_sw128(smem_u32(sV), BN * 128, 1024);
       while (ok && next_unit(iu, u)) {
+        const bool pk = kPack && u.pack;
         if (lane == 0) {
           // Per tile, in head order: O_h += P_h V (P from tensor memory) once V
           // is in and the head's P is written; then the S/P buffer and the V
           // slot are released.  A unit's first P.V overwrites O_h, so it also
           // waits until the previous unit's epilogue has read O_h.  Head order
           // keeps every head's last P.V behind warpgroup 0, which clears the V
-          // rows past the context before it publishes its P.
+          // rows past the context before it publishes its P.  A packed unit
+          // has one P.V (both heads' rows) into head 0's O.
           for (int jt = 0; jt < u.n_kv && ok; ++jt, ++g) {
             const int pst = g % kVStages;
             ok = mbar_wait_bounded(&v_full[pst], (g / kVStages) & 1, abort_flag);
             const uint64_t dv_st = dv + (uint64_t)((pst * L::kKVBytes) >> 4);
 #pragma unroll
             for (int h = 0; h < NH && ok; ++h) {
-              ok = mbar_wait_bounded(&p_full[2 * h + (g & 1)], (g >> 1) & 1, abort_flag);
-              if (ok && jt == 0 && iu >= 2)
-                ok = mbar_wait_bounded(&o_free[h], (iu - 2) & 1, abort_flag);
+              if (pk && h > 0) break;
+              const int gh = (kPack && h == 1) ? g1 + jt : g;  // head h's tile count
+              const int uh = (kPack && h == 1) ? u1 : iu - 1;  // head h's units before this one
+              ok = mbar_wait_bounded(&p_full[2 * h + (gh & 1)], (gh >> 1) & 1, abort_flag);
+              if (ok && jt == 0 && uh >= 1)
+                ok = mbar_wait_bounded(&o_free[h], (uh - 1) & 1, abort_flag);
               if (!ok) break;
               tc_fence_after_sync();
-              const uint32_t pa = tmem + kSCol + (2 * h + (g & 1)) * BN;
+              const uint32_t pa = tmem + kSCol + (2 * h + (gh & 1)) * BN;
 #pragma unroll
               for (int kk = 0; kk < BN / 16; ++kk)
                 umma_bf16_tmem_a(tmem + kOCol + h * D, pa + kk * 8,
                                  dv_st + (uint64_t)((kk * 16 * 128) >> 4), idesc_o,
                                  (jt > 0 || kk > 0) ? 1u : 0u);
-              umma_commit(&p_free[2 * h + (g & 1)]);
+              umma_commit(&p_free[2 * h + (gh & 1)]);
             }
             if (ok) umma_commit(&v_empty[pst]);
           }
         }
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         g = __shfl_sync(0xffffffffu, g, 0);
+        if (kPack && !pk) {
+          g1 += u.n_kv;
+          ++u1;
+        }
       }
     }
     if (lane == 0) {
@@ -560,6 +592,9 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     const float qs = p.qscale;
     int iu = 0, g = 0;
+    // Packing kernels: warpgroup 1 takes no part in packed units; its S/P
+    // buffer barriers count only the tiles it processes (g1).
+    int g1 = 0;
     bool ok = true;
     Unit u;
     // Epilogue of a unit (rows from query row e_row0, e_rows of them valid,
@@ -569,16 +604,21 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
     // through g_last's buffer barrier: its use before (tile g_last - 2) was
     // done before S of g_last was computed, and its next use needs a P this
     // warpgroup has not yet written, so the parity wait cannot alias.
-    auto epilogue = [&](int e_row0, int e_rows, int e_h, float l_e, int g_last) -> bool {
+    // In a packed unit (warpgroup 0 only) row r holds query row r % 64 of
+    // head e_h + r / 64.
+    auto epilogue = [&](int e_row0, int e_rows, int e_h, float l_e, int g_last,
+                        bool e_pack) -> bool {
       if (!warp_wait(&p_free[2 * h + (g_last & 1)], (g_last >> 1) & 1, abort_flag)) return false;
       tc_fence_after_sync();
       const float inv = 1.f / l_e;
-      uint16_t *dst = p.out + ((int64_t)(e_row0 + row) * p.num_q_heads + e_h + h) * D;
+      const int orow = (kPack && e_pack) ? (row & (BM / 2 - 1)) : row;
+      const int ohead = (kPack && e_pack) ? (row >> 6) : h;
+      uint16_t *dst = p.out + ((int64_t)(e_row0 + orow) * p.num_q_heads + e_h + ohead) * D;
 #pragma unroll 1
       for (int half = 0; half < D / 64; ++half) {
         float ov[64];
         tmem_load64(tmem + lane_base + kOCol + h * D + half * 64, ov);
-        if (row < e_rows) {
+        if (orow < e_rows) {
 #pragma unroll
           for (int i = 0; i < 64; i += 16) {
             uint32_t w[8];
@@ -604,9 +644,20 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
     };
     bool pending = false;  // a unit's epilogue is still to run
     int e_row0 = 0, e_rows = 0, e_h = 0, e_g = 0;
+    bool e_pack = false;
     float e_l = 0.f;
     while (ok && next_unit(iu, u)) {
-      const int key_limit = min(u.c + u.q0 + row, u.len_k - 1);  // last key this row may see
+      const bool pk = kPack && u.pack;
+      if (pk && h == 1) {  // a packed unit has no work for the second head's warpgroup
+        if (pending) {
+          pending = false;
+          ok = epilogue(e_row0, e_rows, e_h, e_l, e_g, e_pack);
+        }
+        g += u.n_kv;
+        continue;
+      }
+      const int prow = pk ? (row & (BM / 2 - 1)) : row;  // the row's query index in the tile
+      const int key_limit = min(u.c + u.q0 + prow, u.len_k - 1);  // last key this row may see
       // Running max in log2 units.  It is only raised (and O rescaled) when a
       // tile's max exceeds it by more than 8, so P stays <= 2^8; l and O share
       // the same reference, so the final O / l is unchanged.
@@ -614,8 +665,9 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
       float l_run = 0.f;
       for (int jt = 0; jt < u.n_kv && ok; ++jt, ++g) {
         const int key0 = jt * BN;
-        const uint32_t sp = tmem + lane_base + kSCol + (2 * h + (g & 1)) * BN;  // S, then P
-        ok = warp_wait(&s_full[2 * h + (g & 1)], (g >> 1) & 1, abort_flag);
+        const int gt = (kPack && h == 1) ? g1 + jt : g;  // this warpgroup's S/P buffer turns
+        const uint32_t sp = tmem + lane_base + kSCol + (2 * h + (gt & 1)) * BN;  // S, then P
+        ok = warp_wait(&s_full[2 * h + (gt & 1)], (gt >> 1) & 1, abort_flag);
         if (!ok) break;
         tc_fence_after_sync();
         float sv[BN];
@@ -626,7 +678,7 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
         // decode row, a prompt's ragged last tile) skips the arithmetic and
         // the P store: those rows' outputs are never written, and P of a row
         // only reaches that row of O.  It still takes part in every barrier.
-        const bool live = quarter * 32 < u.rows_valid;
+        const bool live = (pk ? ((quarter * 32) & (BM / 2 - 1)) : quarter * 32) < u.rows_valid;
         if (live) {
           tmem_load64(sp, sv);
           // Tile max of the scaled logits over this row's visible keys (4-way tree).
@@ -707,7 +759,7 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
           // its use before (tile g - 3) was done before S of tile g - 1 was
           // computed, and its next use needs this tile's P, so the parity
           // wait cannot alias.
-          ok = warp_wait(&p_free[2 * h + ((g - 1) & 1)], ((g - 1) >> 1) & 1, abort_flag);
+          ok = warp_wait(&p_free[2 * h + ((gt - 1) & 1)], ((gt - 1) >> 1) & 1, abort_flag);
           if (!ok) break;
           tc_fence_after_sync();
 #pragma unroll 1
@@ -753,10 +805,10 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
           tmem_store32(sp, pw);
         }
         tc_fence_before_sync();
-        mbar_arrive(&p_full[2 * h + (g & 1)]);
+        mbar_arrive(&p_full[2 * h + (gt & 1)]);
         if (pending) {  // the previous unit's epilogue, after this unit's first P
           pending = false;
-          ok = epilogue(e_row0, e_rows, e_h, e_l, e_g);
+          ok = epilogue(e_row0, e_rows, e_h, e_l, e_g, e_pack);
         }
       }
       if (!ok) break;
@@ -765,9 +817,11 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
       e_rows = u.rows_valid;
       e_h = u.h_first;
       e_l = l_run;
-      e_g = g - 1;
+      e_g = ((kPack && h == 1) ? g1 + u.n_kv : g) - 1;
+      e_pack = pk;
+      if (kPack && h == 1) g1 += u.n_kv;
     }
-    if (ok && pending) ok = epilogue(e_row0, e_rows, e_h, e_l, e_g);
+    if (ok && pending) ok = epilogue(e_row0, e_rows, e_h, e_l, e_g, e_pack);
     tc_fence_before_sync();
   }
 
@@ -779,9 +833,9 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
   }
 }
 
-template <int D, int NH>
-pkv_status launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                          const PrefillParams &prm, cudaStream_t stream) {
+template <int D, int NH, bool kPack>
+pkv_status launch_prefill(const CUtensorMap &tq, const CUtensorMap &tq64, const CUtensorMap &tk,
+                          const CUtensorMap &tv, const PrefillParams &prm, cudaStream_t stream) {
   using L = PrefillLayout<D, NH>;
   int smem = L::total + 1024;
   // Resident CTAs per SM must not ask for more than 512 TMEM columns in
@@ -791,7 +845,7 @@ pkv_status launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const CU
   const int min_bytes = per_sm / (max_ctas + 1) + 1;
   if (smem < min_bytes) smem = min_bytes;
   int resident = 0;
-  if (!kernel_smem_setup((const void *)paged_prefill_kernel<D, NH>, threads_for<NH>(), smem,
+  if (!kernel_smem_setup((const void *)paged_prefill_kernel<D, NH, kPack>, threads_for<NH>(), smem,
                          &resident))
     return PKV_ERR_CUDA;
   // Persistent: as many CTAs as can be resident, no more than there are units.
@@ -799,7 +853,8 @@ pkv_status launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const CU
   int64_t grid = (int64_t)device_sm_count() * ctas_per_sm;
   if (grid > (int64_t)prm.num_units) grid = prm.num_units;
   if (grid < 1) grid = 1;
-  paged_prefill_kernel<D, NH><<<(unsigned)grid, threads_for<NH>(), smem, stream>>>(tq, tk, tv, prm);
+  paged_prefill_kernel<D, NH, kPack>
+      <<<(unsigned)grid, threads_for<NH>(), smem, stream>>>(tq, tq64, tk, tv, prm);
   return launch_status();
 }
 
@@ -876,15 +931,33 @@ extern "C" pkv_status pkv_paged_prefill_attn(uint16_t *out, const uint16_t *q,
   const uint64_t kstr[3] = {(uint64_t)head_dim * 2, (uint64_t)num_kv_heads * head_dim * 2,
                             (uint64_t)block_size * num_kv_heads * head_dim * 2};
   const uint32_t kbox[4] = {64u, 1u, (uint32_t)BN, 1u};
-  CUtensorMap tq, tk, tv;
+  // Decode-heavy batches (at most kPackMeanQ new tokens per sequence on
+  // average, none over kPackMaxQ) run the packing kernel: its query tiles
+  // with at most 64 valid rows (decode rows, short prompts, ragged last
+  // tiles) hold both heads of the pair, 64 rows each, in one 128-row MMA
+  // tile (one S and one P.V per key tile instead of two).  Measured: the
+  // mixed step (48 decode rows + 8 chunks) 117.6 -> 112.7 us; on the
+  // prefix-cached batch (19 % of its work packable) the packing kernel's
+  // other units ran slower and the whole call went 78.4 -> 81.2 us, so
+  // batches like it keep the kernel without the path.
+  const bool pack = two_heads && max_seqlen_q <= kPackMaxQ &&
+                    total_q <= (int64_t)kPackMeanQ * num_seqs;
+  const uint32_t qbox64[3] = {64u, 1u, (uint32_t)(BM / 2)};
+  CUtensorMap tq, tq64, tk, tv;
+  if (pack && !encode_bf16_map(&tq64, q, 3, qdims, qstr, qbox64, true)) return PKV_ERR_CUDA;
   if (!encode_bf16_map(&tq, q, 3, qdims, qstr, qbox, true) ||
       !encode_bf16_map(&tk, k_cache, 4, kdims, kstr, kbox, true) ||
       !encode_bf16_map(&tv, v_cache, 4, kdims, kstr, kbox, true))
     return PKV_ERR_CUDA;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (head_dim == 128) return two_heads ? launch_prefill<128, 2>(tq, tk, tv, prm, st)
-                                        : launch_prefill<128, 1>(tq, tk, tv, prm, st);
-  return two_heads ? launch_prefill<64, 2>(tq, tk, tv, prm, st)
-                   : launch_prefill<64, 1>(tq, tk, tv, prm, st);
+  if (!pack) tq64 = tq;  // (not read)
+  if (head_dim == 128) {
+    if (!two_heads) return launch_prefill<128, 1, false>(tq, tq64, tk, tv, prm, st);
+    return pack ? launch_prefill<128, 2, true>(tq, tq64, tk, tv, prm, st)
+                : launch_prefill<128, 2, false>(tq, tq64, tk, tv, prm, st);
+  }
+  if (!two_heads) return launch_prefill<64, 1, false>(tq, tq64, tk, tv, prm, st);
+  return pack ? launch_prefill<64, 2, true>(tq, tq64, tk, tv, prm, st)
+              : launch_prefill<64, 2, false>(tq, tq64, tk, tv, prm, st);
 }

@@ -49,6 +49,22 @@ def test_prefill_single_row_units(lib, D, G):
     assert torch.isfinite(out.float()).all()
 
 
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("G", [2, 4, 8])
+def test_prefill_packed_tiles(lib, D, G):
+    # A decode-heavy batch (mean new tokens per sequence <= 128) runs the
+    # packing kernel: tiles with at most 64 valid rows hold both heads of a
+    # pair, 64 rows each.  Tails of 1, 31, 32, 33, 63, 64 and 65 rows (the
+    # packing limit and the warp boundaries), short prompts, decode rows and
+    # full tiles in one launch, over cached prefixes, NaN in stale slots.
+    new = [1] * 24 + [129, 159, 160, 161, 191, 192, 193, 64, 65, 33, 256]
+    cached = [(37 * i) % 700 for i in range(len(new))]
+    b = wl.build_batch("packed", "prefill", 110 + D + G, cached, new, 2 * G, 2, D, stale="nan")
+    assert b.q.shape[0] <= 128 * b.num_seqs and max(new) <= 1024
+    db, out = check_prefill(lib, b)
+    assert torch.isfinite(out.float()).all()
+
+
 def test_prefill_single_row_of_context_one_returns_v_bits(lib):
     b = wl.build_batch("one1", "prefill", 79, [0, 0, 0], [1, 1, 1], 8, 4, 128)
     db = DeviceBatch(lib, b)
