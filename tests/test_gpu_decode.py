@@ -64,6 +64,24 @@ def test_decode_batch_of_4096_sequences(lib):
     check_decode(lib, b)
 
 
+def test_decode_merge_paths_agree_at_the_batch_size_boundary(lib):
+    # Up to 128 sequences the merge finds each sequence's partials from
+    # context_lens itself; from 129 on it reads the prefix the split-K grid
+    # publishes.  The first 128 sequences must come out bit-identical.
+    rng = np.random.default_rng(47)
+    L = rng.integers(1, 1200, size=129, endpoint=True)
+    b = wl.build_batch("edge129", "decode", 47, L - 1, np.ones(129, np.int64), 4, 2, 128, rng=rng)
+    db129, out129 = check_decode(lib, b)
+    mtb = int(b.total_blocks_used)
+    ws = lib.decode_workspace(128, b.num_q_heads, b.num_kv_heads, b.head_dim, mtb, db129.dev)
+    out128 = torch.empty((128, b.num_q_heads, b.head_dim), dtype=torch.bfloat16, device=db129.dev)
+    lib.paged_decode_attn(out128, db129.q[:128], db129.k_cache, db129.v_cache,
+                          db129.block_tables[:128].contiguous(), db129.context_lens[:128].contiguous(),
+                          b.scale, ws, mtb, db129.status)
+    assert db129.status_value() == 0
+    assert np.array_equal(bits(out128), bits(out129[:128]))
+
+
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("G", [1, 2, 4, 8])
 def test_decode_edge_lengths(lib, D, G):
