@@ -193,9 +193,9 @@ def ncu_traffic(*kernels):
 TRAFFIC_KEYS = {
     "decode": ("paged_decode_kernel<128,2>", "decode_merge_kernel<128,2,1>"),
     "longdecode": ("paged_decode_kernel<128,4>@longdecode", "decode_merge_kernel<128,4,0>@longdecode"),
-    "prefill": ("paged_prefill_kernel<128,2>",),
-    "prefix": ("paged_prefill_kernel<128,2>@prefix",),
-    "mixed": ("paged_prefill_kernel<128,2>@mixed",),
+    "prefill": ("paged_prefill_kernel<128,2,0,0>",),
+    "prefix": ("paged_prefill_kernel<128,2,0,1>@prefix",),
+    "mixed": ("paged_prefill_kernel<128,2,1,0>@mixed",),
 }
 
 

@@ -24,7 +24,10 @@
 //  * Warp 1 issues S_h = Q_h K^T (tcgen05.mma, M=128, N=64, fp32 in tensor
 //    memory, two buffers per head); warp 3 issues O_h += P_h V (M=128, N=D,
 //    P from tensor memory, V MN-major).  Two issuers keep the tensor pipe
-//    fed while either waits on a barrier.  The four control warps take the
+//    fed while either waits on a barrier.  For batches of short prompts the
+//    kernel's other form gives each head its own issuer instead (warp 1:
+//    head 0's S and P.V, warp 3: head 1's), so at the frequent unit
+//    boundaries neither head waits on the other.  The four control warps take the
 //    lowest warp ids: the schedulers favour them over the softmax warps
 //    they share a sub-partition with (measured 1-3 % faster than placing
 //    them after the softmax warps, 10 % faster than all four last).
