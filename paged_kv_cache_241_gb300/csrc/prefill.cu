@@ -518,13 +518,14 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
         auto issue_pv = [&]() -> bool {
           const int pst = pg % kVStages;
           if (!mbar_wait_bounded(&v_full[pst], (pg / kVStages) & 1, abort_flag)) return false;
-          if (!mbar_wait_bounded(&p_full[2 * h + (pgh & 1)], (pgh >> 1) & 1, abort_flag)) return false;
+          if (!mbar_wait_bounded(&p_full[2 * h + (pgh & 1)], (pgh >> 1) & 1, abort_flag))
+            return false;
           if (pfirst && puh >= 1 && !mbar_wait_bounded(&o_free[h], (puh - 1) & 1, abort_flag))
             return false;
           tc_fence_after_sync();
           const uint64_t dv_st = dv + (uint64_t)((pst * L::kKVBytes) >> 4);
           const uint32_t pa = tmem + kSCol + (2 * h + (pgh & 1)) * BN;
-  #pragma unroll
+#pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
             umma_bf16_tmem_a(tmem + kOCol + h * D, pa + kk * 8,
                              dv_st + (uint64_t)((kk * 16 * 128) >> 4), idesc_o,
@@ -550,7 +551,8 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
                 const int gg = g + jt;
                 ok = mbar_wait_bounded(&k_full[gg % kKStages], (gg / kKStages) & 1, abort_flag);
                 if (ok) mbar_arrive(&k_empty[gg % kKStages]);
-                if (ok) ok = mbar_wait_bounded(&v_full[gg % kVStages], (gg / kVStages) & 1, abort_flag);
+                if (ok)
+                  ok = mbar_wait_bounded(&v_full[gg % kVStages], (gg / kVStages) & 1, abort_flag);
                 if (ok) mbar_arrive(&v_empty[gg % kVStages]);
               }
               if (ok) mbar_arrive(q_empty);
@@ -568,7 +570,7 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
                 tc_fence_after_sync();
                 const uint64_t dk_st = dk + (uint64_t)((st * L::kKVBytes) >> 4);
                 const uint32_t d = tmem + kSCol + (2 * h + b) * BN;
-  #pragma unroll
+#pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                   const uint32_t off = (kk & 3) * 32;
                   umma_bf16(d, dq + (uint64_t)((h * L::kQBytes + (kk / 4) * BM * 128 + off) >> 4),
@@ -631,16 +633,17 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
               const int st = g % kKStages;
               ok = mbar_wait_bounded(&k_full[st], (g / kKStages) & 1, abort_flag);
               const uint64_t dk_st = dk + (uint64_t)((st * L::kKVBytes) >> 4);
-  #pragma unroll
+#pragma unroll
               for (int h = 0; h < NH && ok; ++h) {
                 if (pk && h > 0) break;
                 const int gh = (kPack && h == 1) ? g1 + jt : g;  // head h's tile count
                 const int b = gh & 1;
-                if (gh >= 2) ok = mbar_wait_bounded(&p_free[2 * h + b], ((gh - 2) >> 1) & 1, abort_flag);
+                if (gh >= 2)
+                  ok = mbar_wait_bounded(&p_free[2 * h + b], ((gh - 2) >> 1) & 1, abort_flag);
                 if (!ok) break;
                 tc_fence_after_sync();
                 const uint32_t d = tmem + kSCol + (2 * h + b) * BN;
-  #pragma unroll
+#pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                   const uint32_t off = (kk & 3) * 32;
                   umma_bf16(d, dq + (uint64_t)((h * L::kQBytes + (kk / 4) * BM * 128 + off) >> 4),
@@ -674,7 +677,7 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
               const int pst = g % kVStages;
               ok = mbar_wait_bounded(&v_full[pst], (g / kVStages) & 1, abort_flag);
               const uint64_t dv_st = dv + (uint64_t)((pst * L::kKVBytes) >> 4);
-  #pragma unroll
+#pragma unroll
               for (int h = 0; h < NH && ok; ++h) {
                 if (pk && h > 0) break;
                 const int gh = (kPack && h == 1) ? g1 + jt : g;  // head h's tile count
@@ -685,7 +688,7 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
                 if (!ok) break;
                 tc_fence_after_sync();
                 const uint32_t pa = tmem + kSCol + (2 * h + (gh & 1)) * BN;
-  #pragma unroll
+#pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
                   umma_bf16_tmem_a(tmem + kOCol + h * D, pa + kk * 8,
                                    dv_st + (uint64_t)((kk * 16 * 128) >> 4), idesc_o,
