@@ -118,10 +118,11 @@ size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads
  * g = Hq / Hkv.  bf16 in, fp32 accumulation, bf16 out (round to nearest even).
  *
  * Split-K flash-decoding: each (sequence, kv head, block) is one work item
+ * (two consecutive blocks per item when the batch has very many of them)
  * whose partial (max, sum, unnormalised output) goes to the workspace; the
  * persistent CTAs take items from a counter in the workspace as they become
  * free.  A second kernel, launched as a programmatic dependent of the first,
- * merges the partials of every sequence that spans more than one block.  Two
+ * merges the partials of every sequence that spans more than one item.  Two
  * kernel launches per call (one when max_blocks_per_seq == 1).
  *
  * workspace: device buffer of at least pkv_decode_workspace_size(...) bytes,
@@ -135,7 +136,7 @@ size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads
  * {64, 128, 256, 512}; num_seqs <= 16384, and the kernel's per-CTA shared
  * memory (which holds every sequence's block offset and length) must fit in
  * 227 KiB: only head_dim 128 with Hq/Hkv 8 and block_size 512 reaches that
- * limit first, at 16097 sequences.  A batch beyond either limit returns
+ * limit first, at 16093 sequences.  A batch beyond either limit returns
  * PKV_ERR_UNSUPPORTED; sizes whose workspace cannot be addressed return
  * PKV_ERR_INVALID_ARG.  Both launch nothing.
  */

@@ -16,8 +16,13 @@
 //    is ready for it, so the CTAs finish together although items and SMs
 //    differ in speed; with few, round-robin (the counter's round trip then
 //    costs more than the balance gains).  The last CTA to finish leaves the
-//    counter zeroed for the next call.
-//  * One producer warp streams the item's K tiles, then its V tiles, as 4-D
+//    counter zeroed for the next call.  When there are very many items (24
+//    or more per CTA, long contexts) and the host launches the kernel's
+//    two-block form, an item spans two consecutive blocks of its sequence:
+//    half the partials to write and merge and half the per-item costs (long
+//    skewed decode 354.6 -> 347.1 us); the consumers carry the running max,
+//    sum and unnormalised O from one block to the next.
+//  * One producer warp streams each block's K tiles, then its V tiles, as 4-D
 //    TMA boxes {D, 1 head, 64 tokens, 1 block} into a ring of shared-memory
 //    stages; the block-table lookup is the box's outer coordinate.  With a
 //    4-deep ring every other slot is filled instead by cp.async from the
@@ -30,9 +35,9 @@
 //    output dims.
 //  * Each item writes a partial (max, sum, unnormalised output) to the
 //    workspace; a merge kernel, launched as a programmatic dependent of this
-//    grid (it waits for the grid's completion), combines each multi-block
+//    grid (it waits for the grid's completion), combines each multi-item
 //    (sequence, kv head)'s partials in parallel and writes bf16.  A sequence
-//    that fits one block skips the workspace.
+//    that fits one item skips the workspace.
 #include <math.h>
 
 #include <mutex>
@@ -55,6 +60,9 @@ constexpr int kItemSlots = 4;       // depth of the shared ring of fetched item 
 // round-robin: measured, long skewed decode (33 per CTA) 365 -> 351 us with
 // the counter, the 64-sequence decode batch (6 per CTA) 60.1 -> 61.2 us.
 constexpr int kCounterRounds = 12;
+// Items per CTA (of one block each) from which an item spans two blocks of
+// its sequence: half the partials to write and merge, half the per-item costs.
+constexpr int kSpanRounds = 24;
 
 // Test-only fault injection, set by pkv_test_decode_fault: the producer of
 // every CTA skips the tile it would issue as its number `withhold` (counting
@@ -82,6 +90,10 @@ struct DecodeParams {
   int block_size;
   int max_blocks_per_seq;
   float qscale;  // scale * log2(e)
+  // Two-block form only: items may span two blocks (the host sets it when it
+  // launches that form; a run-time flag rather than a constant because ptxas
+  // then allocates the form's registers without a spill).
+  int span_ok;
   // Fused store (all null unless the call also stores this step's tokens):
   // row s of new_k / new_v is the token at position context_lens[s] - 1 of
   // sequence s, to be written to cache slot new_slots[s].
@@ -234,7 +246,7 @@ struct DecodeSmem {
     logits = bars + (2 * stages + 4 + 2 * kItemSlots) * 8;  // [block_size][G] float pairs
     red = logits + ((bs * G * 8 + 15) & ~15);
     stats = red + kConsumerWarps * G * D * 4;
-    misc = stats + 2 * G * 4;
+    misc = stats + 3 * G * 4;
     iring = misc + 16;                      // [R] fetched item indices
     prefix = iring + kItemSlots * 4;
     ctx = prefix + (num_seqs + 1) * 4;
@@ -252,8 +264,8 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
       : "memory");
 }
 
-template <int D, int G>
-__global__ void __launch_bounds__(kThreads)
+template <int D, int G, bool kSpan>
+__global__ void __launch_bounds__(kThreads, G < 8 ? 3 : 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
   constexpr int kStages = decode_stages(G);
@@ -282,6 +294,7 @@ __global__ void __launch_bounds__(kThreads)
   float *red = reinterpret_cast<float *>(smem + lay.red);        // [warps][G][D]
   float *mstat = reinterpret_cast<float *>(smem + lay.stats);    // [G]
   float *lstat = mstat + G;                                      // [G]
+  float *astat = lstat + G;  // [G]: factor for what earlier blocks of the item left in O
   int *misc = reinterpret_cast<int *>(smem + lay.misc);          // abort flag
   int *prefix = reinterpret_cast<int *>(smem + lay.prefix);      // [num_seqs + 1]
   int *ctx = reinterpret_cast<int *>(smem + lay.ctx);            // [num_seqs], clamped
@@ -356,17 +369,52 @@ __global__ void __launch_bounds__(kThreads)
   // Block 0 publishes the prefix for the merge kernel (all zeros, i.e. nothing
   // to merge, when the workspace bound is exceeded).
   const bool overflow = (int64_t)total > p.max_total_blocks;
-  if (blockIdx.x == 0)
-    for (int i = tid; i <= S; i += kThreads) p.seq_prefix[i] = overflow ? 0 : prefix[i];
   if (overflow) {
+    if (blockIdx.x == 0)
+      for (int i = tid; i <= S; i += kThreads) p.seq_prefix[i] = 0;
     if (blockIdx.x == 0 && tid == 0) flag_status(p.status, PKV_DEV_WORKSPACE);
     return;
   }
-  const int total_items = total * Hkv;
+  // With many items per CTA an item spans two blocks: the prefix then counts
+  // items of each sequence (its partials), ceil(blocks / 2).
+  const int span = (kSpan && p.span_ok && total * Hkv >= kSpanRounds * (int)gridDim.x) ? 2 : 1;
+  int total_parts = total;
+  if (span == 2) {
+    int lp = 0;
+    for (int s = s_begin; s < s_end; ++s) lp += ((ctx[s] + BS - 1) / BS + 1) >> 1;
+    int ip = lp;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, ip, o);
+      if (lane >= o) ip += y;
+    }
+    if (lane == 31) red[warp] = __int_as_float(ip);
+    __syncthreads();
+    int off2 = ip - lp;
+    int tot2 = 0;
+    for (int w = 0; w < kThreads / 32; ++w) {
+      const int wt = __float_as_int(red[w]);
+      if (w < warp) off2 += wt;
+      tot2 += wt;
+    }
+    int run = off2;
+    for (int s = s_begin; s < s_end; ++s) {
+      prefix[s] = run;
+      run += ((ctx[s] + BS - 1) / BS + 1) >> 1;
+    }
+    if (tid == 0) prefix[S] = tot2;
+    total_parts = tot2;
+    __syncthreads();
+  }
+  if (blockIdx.x == 0)
+    for (int i = tid; i <= S; i += kThreads) p.seq_prefix[i] = prefix[i];
+  const int total_items = total_parts * Hkv;
   // The merge kernel may start launching now; it waits for this grid to finish.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-  auto item_coords = [&](int w, int &s, int &b, int &j, int &gblk) {
+  // Item w: sequence s, kv head j, its first block b and its blocks nbi
+  // (one, or two when items span two blocks), and its partial's index gblk.
+  auto item_coords = [&](int w, int &s, int &b, int &nbi, int &j, int &gblk) {
     gblk = w / Hkv;
     j = w - gblk * Hkv;
     int lo = 0, hi = S - 1;
@@ -378,7 +426,8 @@ __global__ void __launch_bounds__(kThreads)
         hi = mid - 1;
     }
     s = lo;
-    b = gblk - prefix[s];
+    b = (gblk - prefix[s]) * span;
+    nbi = kSpan ? min(span, (ctx[s] + BS - 1) / BS - b) : 1;
   };
 
   // Producer side of the item ring (lane 0 of the producer warp): the next
@@ -419,11 +468,11 @@ __global__ void __launch_bounds__(kThreads)
       int issued = 0;
       int item_no = 0;
       bool ok = true;
-      int s, b, j, gblk;
+      int s, b, nbi, j, gblk;
       int w = fetch_item();
       int blk_next = 0;
       if (w < total_items) {
-        item_coords(w, s, b, j, gblk);
+        item_coords(w, s, b, nbi, j, gblk);
         blk_next = p.block_tables[(int64_t)s * p.max_blocks_per_seq + b];
       }
       for (;; ++item_no) {
@@ -433,14 +482,7 @@ __global__ void __launch_bounds__(kThreads)
         }
         if (w >= total_items) break;
         const int wn = fetch_item();  // the next item (its value is first needed below)
-        item_coords(w, s, b, j, gblk);
-        int blk = blk_next;
-        if (blk < 0 || (int64_t)blk >= p.num_blocks) {
-          flag_status(p.status, PKV_DEV_BAD_BLOCK);
-          blk = 0;
-        }
-        const int valid = min(BS, ctx[s] - b * BS);
-        const int ntile = (valid + kTile - 1) / kTile;
+        item_coords(w, s, b, nbi, j, gblk);
         const int qb = item_no & 1;
         if (item_no >= 2 &&
             !mbar_wait_bounded(&q_empty[qb], ((item_no >> 1) - 1) & 1, abort_flag)) {
@@ -450,6 +492,14 @@ __global__ void __launch_bounds__(kThreads)
         mbar_arrive_expect_tx(&q_full[qb], kQBytes);
         bulk_load(qbuf + qb * kQBytes, p.q + ((int64_t)s * Hq + j * G) * D, kQBytes,
                   &q_full[qb]);
+        for (int bi = 0; bi < nbi && ok; ++bi) {
+        int blk = bi == 0 ? blk_next : p.block_tables[(int64_t)s * p.max_blocks_per_seq + b + bi];
+        if (blk < 0 || (int64_t)blk >= p.num_blocks) {
+          flag_status(p.status, PKV_DEV_BAD_BLOCK);
+          blk = 0;
+        }
+        const int valid = min(BS, ctx[s] - (b + bi) * BS);
+        const int ntile = (valid + kTile - 1) / kTile;
         for (int half = 0; half < 2 && ok; ++half) {
           const CUtensorMap *map = half ? &tm_v : &tm_k;
           for (int t = 0; t < ntile; ++t) {
@@ -467,14 +517,15 @@ __global__ void __launch_bounds__(kThreads)
             ++issued;
           }
         }
+        }
         if (!ok) {
           ++item_no;  // this item's q copy was issued: the drain below waits for it
           break;
         }
         w = wn;
         if (w < total_items) {  // the next item's block id, read early
-          int sn, bn, jn, gn;
-          item_coords(w, sn, bn, jn, gn);
+          int sn, bn, nn, jn, gn;
+          item_coords(w, sn, bn, nn, jn, gn);
           blk_next = p.block_tables[(int64_t)sn * p.max_blocks_per_seq + bn];
         }
       }
@@ -501,12 +552,12 @@ __global__ void __launch_bounds__(kThreads)
     int issued = 0;
     int item_no = 0;
     bool ok = true;
-    int s, b, j, gblk;
+    int s, b, nbi, j, gblk;
     int blk_next = 0;
     int w = lane == 0 ? fetch_item() : 0;
     w = __shfl_sync(0xffffffffu, w, 0);
     if (w < total_items) {
-      item_coords(w, s, b, j, gblk);
+      item_coords(w, s, b, nbi, j, gblk);
       blk_next = p.block_tables[(int64_t)s * p.max_blocks_per_seq + b];
     }
     for (;; ++item_no) {
@@ -517,14 +568,7 @@ __global__ void __launch_bounds__(kThreads)
       }
       if (w >= total_items) break;
       const int wn_lane0 = lane == 0 ? fetch_item() : 0;  // the next item, first needed below
-      item_coords(w, s, b, j, gblk);
-      int blk = blk_next;
-      if (blk < 0 || (int64_t)blk >= p.num_blocks) {
-        if (lane == 0) flag_status(p.status, PKV_DEV_BAD_BLOCK);
-        blk = 0;
-      }
-      const int valid = min(BS, ctx[s] - b * BS);
-      const int ntile = (valid + kTile - 1) / kTile;
+      item_coords(w, s, b, nbi, j, gblk);
       const int qb = item_no & 1;
       if (item_no >= 2) {
         const bool good =
@@ -537,6 +581,14 @@ __global__ void __launch_bounds__(kThreads)
         bulk_load(qbuf + qb * kQBytes, p.q + ((int64_t)s * Hq + j * G) * D, kQBytes,
                   &q_full[qb]);
       }
+      for (int bi = 0; bi < nbi && ok; ++bi) {
+      int blk = bi == 0 ? blk_next : p.block_tables[(int64_t)s * p.max_blocks_per_seq + b + bi];
+      if (blk < 0 || (int64_t)blk >= p.num_blocks) {
+        if (lane == 0) flag_status(p.status, PKV_DEV_BAD_BLOCK);
+        blk = 0;
+      }
+      const int valid = min(BS, ctx[s] - (b + bi) * BS);
+      const int ntile = (valid + kTile - 1) / kTile;
       for (int half = 0; half < 2 && ok; ++half) {
         const CUtensorMap *map = half ? &tm_v : &tm_k;
         const uint16_t *cache = half ? p.v_cache_r : p.k_cache_r;
@@ -570,14 +622,15 @@ __global__ void __launch_bounds__(kThreads)
           ++issued;
         }
       }
+      }
       if (!ok) {
         ++item_no;  // this item's q copy was issued: the drain below waits for it
         break;
       }
       w = __shfl_sync(0xffffffffu, wn_lane0, 0);
       if (w < total_items) {  // the next item's block id, read early
-        int sn, bn, jn, gn;
-        item_coords(w, sn, bn, jn, gn);
+        int sn, bn, nn, jn, gn;
+        item_coords(w, sn, bn, nn, jn, gn);
         blk_next = p.block_tables[(int64_t)sn * p.max_blocks_per_seq + bn];
       }
     }
@@ -616,174 +669,210 @@ __global__ void __launch_bounds__(kThreads)
         break;
       }
     }
-    int s, b, j, gblk;
-    item_coords(w, s, b, j, gblk);
-    const int valid = min(BS, ctx[s] - b * BS);
-    const int ntile = (valid + kTile - 1) / kTile;
-    const int nblk = prefix[s + 1] - prefix[s];
+    int s, b, nbi, j, gblk;
+    item_coords(w, s, b, nbi, j, gblk);
+    const int nblk = prefix[s + 1] - prefix[s];  // the sequence's items (partials)
+    const int nb_seq = (ctx[s] + BS - 1) / BS;   // and its blocks
     const int h0 = j * G;
 
-    // Fused store: the item that holds the sequence's newest token takes that
-    // token's K/V row from the inputs (patched into its shared-memory tiles,
-    // so it never depends on the cache write) and stores it to the cache once
-    // its tiles are consumed.  pl = the token's index inside this block.
-    int pl = -1;
-    uint4 new_krow = make_uint4(0, 0, 0, 0), new_vrow = make_uint4(0, 0, 0, 0);
-    if (p.new_k != nullptr && b == nblk - 1 && ctx[s] == p.context_lens[s]) {
-      pl = ctx[s] - 1 - b * BS;
-      if (lane < D / 8) {
-        const int64_t row = ((int64_t)s * Hkv + j) * D + lane * 8;
-        new_krow = __ldg(reinterpret_cast<const uint4 *>(p.new_k + row));
-        new_vrow = __ldg(reinterpret_cast<const uint4 *>(p.new_v + row));
-      }
-    }
+    // q of the item, staged by the producer (slot item_no & 1); read again
+    // for each of the item's blocks and released after the last.
+    const int qb = item_no & 1;
+    const bool q_ok = mbar_wait_bounded(&q_full[qb], (item_no >> 1) & 1, abort_flag);
+    const uint16_t *qs = reinterpret_cast<const uint16_t *>(qbuf + qb * kQBytes);
 
-    // q fragment from the staged copy: dim pairs (2e, 2e+1) of chunks r + 8c,
-    // in log2 units.
-    float2 qf[G][CPL * 4];
-    {
-      const int qb = item_no & 1;
-      const bool ok = mbar_wait_bounded(&q_full[qb], (item_no >> 1) & 1, abort_flag);
-      const uint16_t *qs = reinterpret_cast<const uint16_t *>(qbuf + qb * kQBytes);
+    // O accumulates over the item's blocks (unnormalised); between blocks
+    // each warp keeps its share in its part of the reduction area.
+    float2 acc_o[G][DPL / 2];
+    for (int bi = 0; bi < nbi; ++bi) {
+      const int bb = b + bi;
+      const int valid = min(BS, ctx[s] - bb * BS);
+      const int ntile = (valid + kTile - 1) / kTile;
+
+      // q fragment: dim pairs (2e, 2e+1) of chunks r + 8c, in log2 units.
+      float2 qf[G][CPL * 4];
 #pragma unroll
       for (int h = 0; h < G; ++h) {
 #pragma unroll
         for (int c = 0; c < CPL; ++c) {
           uint4 raw = make_uint4(0, 0, 0, 0);
-          if (ok) raw = *reinterpret_cast<const uint4 *>(qs + h * D + (r + 8 * c) * 8);
+          if (q_ok) raw = *reinterpret_cast<const uint4 *>(qs + h * D + (r + 8 * c) * 8);
           const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e)
             qf[h][c * 4 + e] = make_float2(bf16lo(wv[e]) * p.qscale, bf16hi(wv[e]) * p.qscale);
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&q_empty[qb]);
-    }
+      if (bi == nbi - 1) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&q_empty[qb]);
+      }
 
-    // Phase 1: logits of the item's tokens.
-    for (int t = 0; t < ntile; ++t, ++ctile) {
-      const int st = ctile % kStages;
-      const bool ok = mbar_wait_bounded(&full[st], (ctile / kStages) & 1, abort_flag);
-      if (ok) {
-        const uint16_t *tile = reinterpret_cast<const uint16_t *>(tiles + st * kTileBytes);
-        const int tok0 = warp * 16 + gid * 4;
-        if (pl >= 0 && (pl >> 6) == t && warp == ((pl & 63) >> 4)) {
-          if (lane < D / 8)
-            reinterpret_cast<uint4 *>(tiles + st * kTileBytes + (pl & 63) * D * 2)[lane] = new_krow;
-          __syncwarp();
+      // Fused store: the item that holds the sequence's newest token takes that
+      // token's K/V row from the inputs (patched into its shared-memory tiles,
+      // so it never depends on the cache write) and stores it to the cache once
+      // its tiles are consumed.  pl = the token's index inside this block.
+      int pl = -1;
+      uint4 new_krow = make_uint4(0, 0, 0, 0), new_vrow = make_uint4(0, 0, 0, 0);
+      if (p.new_k != nullptr && bb == nb_seq - 1 && ctx[s] == p.context_lens[s]) {
+        pl = ctx[s] - 1 - bb * BS;
+        if (lane < D / 8) {
+          const int64_t row = ((int64_t)s * Hkv + j) * D + lane * 8;
+          new_krow = __ldg(reinterpret_cast<const uint4 *>(p.new_k + row));
+          new_vrow = __ldg(reinterpret_cast<const uint4 *>(p.new_v + row));
         }
-        // Packed FP32x2 FMAs: even and odd dims accumulate in the two halves.
-        float2 acc2[NV];
+      }
+
+      // Phase 1: logits of the item's tokens.
+      for (int t = 0; t < ntile; ++t, ++ctile) {
+        const int st = ctile % kStages;
+        const bool ok = mbar_wait_bounded(&full[st], (ctile / kStages) & 1, abort_flag);
+        if (ok) {
+          const uint16_t *tile = reinterpret_cast<const uint16_t *>(tiles + st * kTileBytes);
+          const int tok0 = warp * 16 + gid * 4;
+          if (pl >= 0 && (pl >> 6) == t && warp == ((pl & 63) >> 4)) {
+            if (lane < D / 8)
+              reinterpret_cast<uint4 *>(tiles + st * kTileBytes + (pl & 63) * D * 2)[lane] = new_krow;
+            __syncwarp();
+          }
+          // Packed FP32x2 FMAs: even and odd dims accumulate in the two halves.
+          float2 acc2[NV];
 #pragma unroll
-        for (int i = 0; i < NV; ++i) acc2[i] = make_float2(0.f, 0.f);
+          for (int i = 0; i < NV; ++i) acc2[i] = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint16_t *krow = tile + (tok0 + i) * D;
+          for (int i = 0; i < 4; ++i) {
+            const uint16_t *krow = tile + (tok0 + i) * D;
 #pragma unroll
-          for (int c = 0; c < CPL; ++c) {
-            const uint4 raw = *reinterpret_cast<const uint4 *>(krow + (r + 8 * c) * 8);
-            const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+            for (int c = 0; c < CPL; ++c) {
+              const uint4 raw = *reinterpret_cast<const uint4 *>(krow + (r + 8 * c) * 8);
+              const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 kk = make_float2(bf16lo(wv[e]), bf16hi(wv[e]));
+              for (int e = 0; e < 4; ++e) {
+                const float2 kk = make_float2(bf16lo(wv[e]), bf16hi(wv[e]));
 #pragma unroll
-              for (int h = 0; h < G; ++h)
-                acc2[i * G + h] = __ffma2_rn(qf[h][c * 4 + e], kk, acc2[i * G + h]);
+                for (int h = 0; h < G; ++h)
+                  acc2[i * G + h] = __ffma2_rn(qf[h][c * 4 + e], kk, acc2[i * G + h]);
+              }
+            }
+          }
+          float acc[NV];
+#pragma unroll
+          for (int i = 0; i < NV; ++i) acc[i] = acc2[i].x + acc2[i].y;
+          octet_reduce<NV>(acc, r);
+          const int base = octet_base<NV>(r);
+          constexpr int kOwned = NV >= 8 ? NV / 8 : 1;
+          if (NV >= 8 || (r & 1) == 0) {
+#pragma unroll
+            for (int u = 0; u < kOwned; ++u) {
+              const int vi = base + u;
+              const int i = vi / G;
+              const int h = vi - i * G;
+              logits[(t * kTile + tok0 + i) * G + h].x = acc[u];
             }
           }
         }
-        float acc[NV];
-#pragma unroll
-        for (int i = 0; i < NV; ++i) acc[i] = acc2[i].x + acc2[i].y;
-        octet_reduce<NV>(acc, r);
-        const int base = octet_base<NV>(r);
-        constexpr int kOwned = NV >= 8 ? NV / 8 : 1;
-        if (NV >= 8 || (r & 1) == 0) {
-#pragma unroll
-          for (int u = 0; u < kOwned; ++u) {
-            const int vi = base + u;
-            const int i = vi / G;
-            const int h = vi - i * G;
-            logits[(t * kTile + tok0 + i) * G + h].x = acc[u];
-          }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+      }
+      named_bar_sync(1, kConsumerWarps * 32);
+
+      // Phase 2: softmax statistics of this block, per head, against the
+      // running max of the item's blocks so far (log2 units); alpha rescales
+      // what the earlier blocks left in O and l.
+      for (int h = warp; h < G; h += kConsumerWarps) {
+        float m = -INFINITY;
+        for (int x = lane; x < valid; x += 32) m = fmaxf(m, logits[x * G + h].x);
+        m = warp_max(m);
+        const float m_old = bi == 0 ? -INFINITY : mstat[h];
+        const float mn = fmaxf(m_old, m);
+        float l = 0.f;
+        for (int x = lane; x < valid; x += 32) {
+          const float e = fast_exp2(logits[x * G + h].x - mn);
+          logits[x * G + h] = make_float2(e, e);
+          l += e;
+        }
+        l = warp_sum(l);
+        if (lane == 0) {
+          const float a = bi == 0 ? 0.f : fast_exp2(m_old - mn);
+          mstat[h] = mn;
+          lstat[h] = (bi == 0 ? 0.f : lstat[h] * a) + l;
+          if constexpr (kSpan) astat[h] = a;
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[st]);
-    }
-    named_bar_sync(1, kConsumerWarps * 32);
-
-    // Phase 2: exact softmax statistics of this item, per head.
-    for (int h = warp; h < G; h += kConsumerWarps) {
-      float m = -INFINITY;
-      for (int x = lane; x < valid; x += 32) m = fmaxf(m, logits[x * G + h].x);
-      m = warp_max(m);
-      float l = 0.f;
-      for (int x = lane; x < valid; x += 32) {
-        const float e = fast_exp2(logits[x * G + h].x - m);
-        logits[x * G + h] = make_float2(e, e);
-        l += e;
-      }
-      l = warp_sum(l);
-      if (lane == 0) {
-        mstat[h] = m;
-        lstat[h] = l;
-      }
-    }
-    named_bar_sync(1, kConsumerWarps * 32);
-
-    // Phase 3: unnormalised P.V, lane owns dims [lane*DPL, lane*DPL + DPL).
-    float2 acc_o[G][DPL / 2];
+      named_bar_sync(1, kConsumerWarps * 32);
 #pragma unroll
-    for (int h = 0; h < G; ++h)
+      for (int h = 0; h < G; ++h) {
+        const float a = kSpan ? astat[h] : 0.f;
 #pragma unroll
-      for (int e = 0; e < DPL / 2; ++e) acc_o[h][e] = make_float2(0.f, 0.f);
-    for (int t = 0; t < ntile; ++t, ++ctile) {
-      const int st = ctile % kStages;
-      const bool ok = mbar_wait_bounded(&full[st], (ctile / kStages) & 1, abort_flag);
-      if (ok) {
-        const uint16_t *tile = reinterpret_cast<const uint16_t *>(tiles + st * kTileBytes);
-        const int tlo = warp * 16;
-        if (pl >= 0 && (pl >> 6) == t && warp == ((pl & 63) >> 4)) {
-          if (lane < D / 8)
-            reinterpret_cast<uint4 *>(tiles + st * kTileBytes + (pl & 63) * D * 2)[lane] = new_vrow;
-          __syncwarp();
-        }
-        const int thi = min(tlo + 16, valid - t * kTile);
-#pragma unroll 4
-        for (int tok = tlo; tok < thi; ++tok) {
-          float2 vf[DPL / 2];
-          if constexpr (DPL == 4) {
-            const uint2 raw = *reinterpret_cast<const uint2 *>(tile + tok * D + lane * 4);
-            vf[0] = make_float2(bf16lo(raw.x), bf16hi(raw.x));
-            vf[1] = make_float2(bf16lo(raw.y), bf16hi(raw.y));
+        for (int e = 0; e < DPL / 2; ++e) {
+          if (!kSpan || bi == 0) {
+            acc_o[h][e] = make_float2(0.f, 0.f);
           } else {
-            const uint32_t raw = *reinterpret_cast<const uint32_t *>(tile + tok * D + lane * 2);
-            vf[0] = make_float2(bf16lo(raw), bf16hi(raw));
+            const float2 o =
+                *reinterpret_cast<const float2 *>(red + (warp * G + h) * D + lane * DPL + 2 * e);
+            acc_o[h][e] = make_float2(o.x * a, o.y * a);
           }
-          float2 pv[G];
-          load_prob_pairs<G>(logits + (t * kTile + tok) * G, pv);
-#pragma unroll
-          for (int h = 0; h < G; ++h)
-#pragma unroll
-            for (int e = 0; e < DPL / 2; ++e) acc_o[h][e] = __ffma2_rn(pv[h], vf[e], acc_o[h][e]);
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[st]);
-    }
 
-    if (pl >= 0 && warp == 0) {
-      const int64_t slot = p.new_slots[s];
-      if (slot >= 0 && slot < p.num_blocks * BS) {
-        if (lane < D / 8) {
-          const int64_t row = (slot * Hkv + j) * D + lane * 8;
-          *reinterpret_cast<uint4 *>(p.k_cache_w + row) = new_krow;
-          *reinterpret_cast<uint4 *>(p.v_cache_w + row) = new_vrow;
+      // Phase 3: unnormalised P.V, lane owns dims [lane*DPL, lane*DPL + DPL).
+      for (int t = 0; t < ntile; ++t, ++ctile) {
+        const int st = ctile % kStages;
+        const bool ok = mbar_wait_bounded(&full[st], (ctile / kStages) & 1, abort_flag);
+        if (ok) {
+          const uint16_t *tile = reinterpret_cast<const uint16_t *>(tiles + st * kTileBytes);
+          const int tlo = warp * 16;
+          if (pl >= 0 && (pl >> 6) == t && warp == ((pl & 63) >> 4)) {
+            if (lane < D / 8)
+              reinterpret_cast<uint4 *>(tiles + st * kTileBytes + (pl & 63) * D * 2)[lane] = new_vrow;
+            __syncwarp();
+          }
+          const int thi = min(tlo + 16, valid - t * kTile);
+#pragma unroll 4
+          for (int tok = tlo; tok < thi; ++tok) {
+            float2 vf[DPL / 2];
+            if constexpr (DPL == 4) {
+              const uint2 raw = *reinterpret_cast<const uint2 *>(tile + tok * D + lane * 4);
+              vf[0] = make_float2(bf16lo(raw.x), bf16hi(raw.x));
+              vf[1] = make_float2(bf16lo(raw.y), bf16hi(raw.y));
+            } else {
+              const uint32_t raw = *reinterpret_cast<const uint32_t *>(tile + tok * D + lane * 2);
+              vf[0] = make_float2(bf16lo(raw), bf16hi(raw));
+            }
+            float2 pv[G];
+            load_prob_pairs<G>(logits + (t * kTile + tok) * G, pv);
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+              for (int e = 0; e < DPL / 2; ++e) acc_o[h][e] = __ffma2_rn(pv[h], vf[e], acc_o[h][e]);
+          }
         }
-      } else if (slot != -1 && lane == 0) {
-        flag_status(p.status, PKV_DEV_BAD_SLOT);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+      }
+
+      if (pl >= 0 && warp == 0) {
+        const int64_t slot = p.new_slots[s];
+        if (slot >= 0 && slot < p.num_blocks * BS) {
+          if (lane < D / 8) {
+            const int64_t row = (slot * Hkv + j) * D + lane * 8;
+            *reinterpret_cast<uint4 *>(p.k_cache_w + row) = new_krow;
+            *reinterpret_cast<uint4 *>(p.v_cache_w + row) = new_vrow;
+          }
+        } else if (slot != -1 && lane == 0) {
+          flag_status(p.status, PKV_DEV_BAD_SLOT);
+        }
+      }
+
+      if (bi + 1 < nbi) {
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+          for (int e = 0; e < DPL / 2; ++e)
+            *reinterpret_cast<float2 *>(red + (warp * G + h) * D + lane * DPL + 2 * e) =
+                acc_o[h][e];
+        // The next block's logits go where this block's probabilities are.
+        named_bar_sync(1, kConsumerWarps * 32);
       }
     }
 
@@ -836,7 +925,7 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-// Split-K merge: one CTA per (sequence, kv head) with more than one block.
+// Split-K merge: one CTA per (sequence, kv head) with more than one item (partial).
 // M = max_b m_b;  O = sum_b 2^(m_b - M) o_b / sum_b 2^(m_b - M) l_b  (log2 units).
 // Threads are split into groups that take interleaved partials; each thread
 // merges its partials in one pass (running max, rescaling what it has so
@@ -865,6 +954,8 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
   const int tid = threadIdx.x;
   int pb0 = 0, nblk = 0;
   if constexpr (kLocal) {
+    // (A local merge always follows the split-K kernel's one-block form, so
+    // a sequence's partials are its blocks.)
     __shared__ int sRed[3][kMergeThreads / 32];
     // context_lens is an input of the call: the split-K grid never writes it.
     int before = 0, total = 0, bad = 0;
@@ -905,7 +996,7 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
   if constexpr (!kLocal) {
     pb0 = p.seq_prefix[s];
     nblk = p.seq_prefix[s + 1] - pb0;
-    if (nblk <= 1) return;  // single-block sequences were finished by the split-K grid
+    if (nblk <= 1) return;  // single-item sequences were finished by the split-K grid
   }
   if (pb0 < 0 || (int64_t)pb0 + nblk > p.max_total_blocks) return;  // never index past the workspace
   const int h0 = j * G;
@@ -968,23 +1059,30 @@ pkv_status launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const Dec
   const DecodeSmem lay(D, G, prm.block_size, prm.num_seqs);
   const int smem = lay.total + 1024;  // + alignment slack
   int ctas_per_sm = 0;
-  if (!kernel_smem_setup((const void *)paged_decode_kernel<D, G>, kThreads, smem, &ctas_per_sm))
-    return PKV_ERR_CUDA;
+  const int64_t merge_grid = (int64_t)prm.num_seqs * prm.num_kv_heads;
   const int sms = device_sm_count();
   if (sms <= 0) return PKV_ERR_CUDA;
+  const bool local =
+      prm.num_seqs <= kMergeLocalSeqs && merge_grid <= (int64_t)kMergeLocalCtasPerSm * sms;
+  // Items may span two blocks only when the merge reads the published prefix
+  // and there can be enough items for it (then the kernel decides).
+  const bool span = !local && max_items >= (int64_t)kSpanRounds * 3 * sms;
+  const void *kfn = span ? (const void *)paged_decode_kernel<D, G, true>
+                         : (const void *)paged_decode_kernel<D, G, false>;
+  if (!kernel_smem_setup(kfn, kThreads, smem, &ctas_per_sm)) return PKV_ERR_CUDA;
   int64_t grid = (int64_t)sms * ctas_per_sm;
   if (grid > max_items) grid = max_items;
   if (grid < 1) grid = 1;
-  paged_decode_kernel<D, G><<<(unsigned)grid, kThreads, smem, stream>>>(tk, tv, prm);
+  if (span)
+    paged_decode_kernel<D, G, true><<<(unsigned)grid, kThreads, smem, stream>>>(tk, tv, prm);
+  else
+    paged_decode_kernel<D, G, false><<<(unsigned)grid, kThreads, smem, stream>>>(tk, tv, prm);
   if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
   if (prm.max_blocks_per_seq <= 1) return PKV_OK;  // nothing can need a merge
   // The merge grid is launched as a programmatic dependent of the split-K
   // grid: it may be scheduled early and waits (griddepcontrol.wait) for the
   // split-K grid's completion before reading the partials.
-  const int64_t merge_grid = (int64_t)prm.num_seqs * prm.num_kv_heads;
   if (merge_grid > 0x7FFFFFFFLL) return PKV_ERR_INVALID_ARG;
-  const bool local =
-      prm.num_seqs <= kMergeLocalSeqs && merge_grid <= (int64_t)kMergeLocalCtasPerSm * sms;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)merge_grid);
   cfg.blockDim = dim3(kMergeThreads);
@@ -1085,6 +1183,7 @@ pkv_status decode_call(uint16_t *out, const uint16_t *q, const uint16_t *k_cache
   prm.block_size = block_size;
   prm.max_blocks_per_seq = max_blocks_per_seq;
   prm.qscale = scale * kLog2e;
+  prm.span_ok = 1;
   prm.new_k = new_k;
   prm.new_v = new_v;
   prm.new_slots = new_slots;

@@ -111,10 +111,10 @@ def test_decode_rejects_bad_arguments(lib):
     assert decode_call(lib, out=p, q=p, kc=p, vc=p, bt=p, cl=p, ws=p, wsb=1 << 40,
                        mtb=1 << 62) == 1
     # the shared-memory layout of the largest group and block size holds at
-    # most 16097 sequences; other shapes reach the 16384-sequence limit first
+    # most 16093 sequences; other shapes reach the 16384-sequence limit first
     big = dict(out=p, q=p, kc=p, vc=p, bt=p, cl=p, Hq=64, Hkv=8, BS=512)
-    assert decode_call(lib, **big, S=16098) == 2
-    assert decode_call(lib, **big, S=16097) == 3          # fits: the (missing) workspace is next
+    assert decode_call(lib, **big, S=16094) == 2
+    assert decode_call(lib, **big, S=16093) == 3          # fits: the (missing) workspace is next
     assert decode_call(lib, out=p, q=p, kc=p, vc=p, bt=p, cl=p, S=16384) == 3
 
 

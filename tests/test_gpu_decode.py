@@ -54,6 +54,22 @@ def test_decode_items_handed_out_by_the_counter(lib, G):
     db, out = check_decode(lib, b)
 
 
+def span_batch(G, seed):
+    """About 20K (sequence, kv head, block) triples over 160 sequences and 4
+    kv heads: items then span two blocks of their sequence (and the merge
+    reads the partials' prefix the split-K grid publishes)."""
+    rng = np.random.default_rng(seed)
+    L = rng.integers(1500, 2500, size=160, endpoint=True)
+    L[:3] = [64, 65, 129]  # one block, two blocks (one item), three blocks (two items)
+    return wl.build_batch("span", "decode", seed, L - 1, np.ones(160, np.int64), 4 * G, 4, 64,
+                          block_size=64, rng=rng)
+
+
+@pytest.mark.parametrize("G", [2, 4])
+def test_decode_items_of_two_blocks(lib, G):
+    check_decode(lib, span_batch(G, 57 + G))
+
+
 def test_decode_batch_of_4096_sequences(lib):
     # A large batch: every CTA keeps all 4096 sequences' block offsets and
     # lengths in shared memory, and the items are handed out by the counter.
@@ -213,7 +229,9 @@ def test_decode_step_replays_from_a_cuda_graph(lib):
     assert_close(out.double().cpu().numpy(), want, "graph replay with new q")
 
 
-@pytest.mark.parametrize("make", [wl.tiny, wl.decode])
+@pytest.mark.parametrize("make", [wl.tiny, wl.decode, lambda: span_batch(2, 61),
+                                  lambda: span_batch(4, 62)],
+                         ids=["tiny", "decode", "span_g2", "span_g4"])
 def test_fused_store_and_decode_match_the_two_calls_bit_for_bit(lib, make):
     b = make()
     two = DeviceBatch(lib, b)            # kv_store, then decode
