@@ -191,8 +191,8 @@ def ncu_traffic(*kernels):
 
 # The counters records of each workload's call (see profiles/counters.json).
 TRAFFIC_KEYS = {
-    "decode": ("paged_decode_kernel<128,2>", "decode_merge_kernel<128,2,1>"),
-    "longdecode": ("paged_decode_kernel<128,4>@longdecode", "decode_merge_kernel<128,4,0>@longdecode"),
+    "decode": ("paged_decode_kernel<128,2,0>", "decode_merge_kernel<128,2,1>"),
+    "longdecode": ("paged_decode_kernel<128,4,1>@longdecode", "decode_merge_kernel<128,4,0>@longdecode"),
     "prefill": ("paged_prefill_kernel<128,2,0,0>",),
     "prefix": ("paged_prefill_kernel<128,2,0,1>@prefix",),
     "mixed": ("paged_prefill_kernel<128,2,1,0>@mixed",),
@@ -828,9 +828,9 @@ def main():
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                      "traffic": ncu_traffic(*TRAFFIC_KEYS["decode"]),
-                     "kernel": ("paged_decode_kernel<128,2> (kv_store fused) + decode_merge_kernel"
+                     "kernel": ("paged_decode_kernel<128,2,0> (kv_store fused) + decode_merge_kernel"
                                 "<128,2,1>" if fused else
-                                "paged_decode_kernel<128,2> + decode_merge_kernel<128,2,1>"),
+                                "paged_decode_kernel<128,2,0> + decode_merge_kernel<128,2,1>"),
                      "bytes_per_launch": kernel_bytes, "peak_source": peak_src,
                      "attn_kernel_ms": attn_ms, "kv_store_ms": store_ms},
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d,
