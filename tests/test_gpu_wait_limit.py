@@ -32,7 +32,16 @@ def many_items(G):
                           block_size=64, rng=rng)
 
 
-@pytest.mark.parametrize("make", [few_items, many_items])
+def two_block_items(G):
+    # ~20K one-block items over 160 sequences and 4 kv heads: the kernel's
+    # two-block form, items of two blocks handed out by the counter
+    rng = np.random.default_rng(97 + G)
+    L = rng.integers(1500, 2500, size=160, endpoint=True)
+    return wl.build_batch("limit", "decode", 97 + G, L - 1, np.ones(160, np.int64), 4 * G, 4, 64,
+                          block_size=64, rng=rng)
+
+
+@pytest.mark.parametrize("make", [few_items, many_items, two_block_items])
 @pytest.mark.parametrize("G", [2, 4])  # 4-stage ring (TMA + cp.async) and 3-stage ring (TMA)
 def test_decode_wait_runs_out_then_next_call_is_correct(lib, G, make):
     b = make(G)
