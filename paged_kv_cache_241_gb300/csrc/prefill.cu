@@ -34,9 +34,12 @@
 //  * Warps 4.. (four per head, one per TMEM lane quarter, the two heads'
 //    warps interleaved so each leads on two sub-partitions; one thread per
 //    query row) read S, apply the causal mask offset by the cached length,
-//    run the online softmax in fp32 (log2 domain), write P as bf16 over the
-//    S it came from, rescale O when the row max grows, and finally
-//    normalise O and store bf16 rows.
+//    run the online softmax in fp32 (log2 domain; a row that sees the whole
+//    key tile gets its max from the TMEM load itself, the load-with-max form
+//    of tcgen05.ld that sm_103a adds), write P as bf16 over the S it came
+//    from (half a tile at a time, each half's store in flight while the
+//    next half's exponentials run), rescale O when the row max grows, and
+//    finally normalise O and store bf16 rows.
 #include <math.h>
 
 #include "host_common.h"
@@ -217,12 +220,6 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
       "mov.b64 {%0, %1}, rd;\n\t}"
       : "=f"(d.x), "=f"(d.y)
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return d;
-}
-// Maximum of three (one instruction).
-__device__ __forceinline__ float max3(float a, float b, float c) {
-  float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
 
@@ -809,28 +806,25 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
         // only reaches that row of O.  It still takes part in every barrier.
         const bool live = (pk ? ((quarter * 32) & (BM / 2 - 1)) : quarter * 32) < u.rows_valid;
         if (live) {
-          tmem_load64(sp, sv);
-          // Tile max of the scaled logits over this row's visible keys (4-way tree).
+          // Tile max of the scaled logits over this row's visible keys: for a
+          // row that sees the whole tile it comes with the TMEM load.
           const bool full_row = key0 + BN - 1 <= key_limit;
           float mt;
           {
-            float e0 = -INFINITY, e1 = -INFINITY, e2 = -INFINITY, e3 = -INFINITY;
+            float e0 = -INFINITY;
             if (qs >= 0.f) {
+              float vmax;
+              tmem_load64_max(sp, sv, vmax);
               if (full_row) {
-#pragma unroll
-                for (int i = 0; i < BN; i += 8) {
-                  e0 = max3(e0, sv[i], sv[i + 1]);
-                  e1 = max3(e1, sv[i + 2], sv[i + 3]);
-                  e2 = max3(e2, sv[i + 4], sv[i + 5]);
-                  e3 = max3(e3, sv[i + 6], sv[i + 7]);
-                }
+                e0 = vmax;
               } else {
 #pragma unroll
                 for (int i = 0; i < BN; ++i)
                   if (key0 + i <= key_limit) e0 = fmaxf(e0, sv[i]);
               }
-              mt = fmaxf(fmaxf(e0, e1), fmaxf(e2, e3)) * qs;
+              mt = e0 * qs;
             } else {
+              tmem_load64(sp, sv);
               e0 = INFINITY;
 #pragma unroll
               for (int i = 0; i < BN; ++i)
@@ -847,39 +841,45 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
             m_ref = m_new;
           }
           {
-            float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
-            if (full_row) {
-              const float2 q2 = make_float2(qs, qs), nm2 = make_float2(-m_ref, -m_ref);
-              float2 r01 = make_float2(0.f, 0.f), r23 = make_float2(0.f, 0.f);
+            // Exponentials in two halves of the tile; each half's P (bf16
+            // pairs, over the first half of this tile's S buffer) is stored
+            // while the next half is computed.
+            const float2 q2 = make_float2(qs, qs), nm2 = make_float2(-m_ref, -m_ref);
+            float2 r01 = make_float2(0.f, 0.f), r23 = make_float2(0.f, 0.f);
 #pragma unroll
-              for (int i = 0; i < BN; i += 4) {
-                const float2 x01 = fma2(make_float2(sv[i], sv[i + 1]), q2, nm2);
-                const float2 x23 = fma2(make_float2(sv[i + 2], sv[i + 3]), q2, nm2);
-                sv[i] = fast_exp2(x01.x);
-                sv[i + 1] = fast_exp2(x01.y);
-                sv[i + 2] = fast_exp2(x23.x);
-                sv[i + 3] = fast_exp2(x23.y);
-                r01 = add2(r01, make_float2(sv[i], sv[i + 1]));
-                r23 = add2(r23, make_float2(sv[i + 2], sv[i + 3]));
+            for (int hf = 0; hf < 2; ++hf) {
+              if (full_row) {
+#pragma unroll
+                for (int i = hf * (BN / 2); i < (hf + 1) * (BN / 2); i += 4) {
+                  const float2 x01 = fma2(make_float2(sv[i], sv[i + 1]), q2, nm2);
+                  const float2 x23 = fma2(make_float2(sv[i + 2], sv[i + 3]), q2, nm2);
+                  sv[i] = fast_exp2(x01.x);
+                  sv[i + 1] = fast_exp2(x01.y);
+                  sv[i + 2] = fast_exp2(x23.x);
+                  sv[i + 3] = fast_exp2(x23.y);
+                  r01 = add2(r01, make_float2(sv[i], sv[i + 1]));
+                  r23 = add2(r23, make_float2(sv[i + 2], sv[i + 3]));
+                }
+              } else {
+#pragma unroll
+                for (int i = hf * (BN / 2); i < (hf + 1) * (BN / 2); i += 4) {
+#pragma unroll
+                  for (int w = 0; w < 4; ++w)
+                    sv[i + w] =
+                        (key0 + i + w <= key_limit) ? fast_exp2(fmaf(sv[i + w], qs, -m_ref)) : 0.f;
+                  r01 = add2(r01, make_float2(sv[i], sv[i + 1]));
+                  r23 = add2(r23, make_float2(sv[i + 2], sv[i + 3]));
+                }
               }
-              r0 = r01.x;
-              r1 = r01.y;
-              r2 = r23.x;
-              r3 = r23.y;
-            } else {
+              float pw[BN / 4];
 #pragma unroll
-              for (int i = 0; i < BN; i += 4) {
-#pragma unroll
-                for (int w = 0; w < 4; ++w)
-                  sv[i + w] =
-                      (key0 + i + w <= key_limit) ? fast_exp2(fmaf(sv[i + w], qs, -m_ref)) : 0.f;
-                r0 += sv[i];
-                r1 += sv[i + 1];
-                r2 += sv[i + 2];
-                r3 += sv[i + 3];
-              }
+              for (int i = 0; i < BN / 4; ++i)
+                pw[i] = __uint_as_float(
+                    pack_bf16x2(sv[hf * (BN / 2) + 2 * i], sv[hf * (BN / 2) + 2 * i + 1]));
+              tmem_store16_async(sp + hf * (BN / 4), pw);
             }
-            rs = (r0 + r1) + (r2 + r3);
+            tmem_wait_st();
+            rs = (r01.x + r01.y) + (r23.x + r23.y);
           }
         }
         if (live && jt > 0 && __any_sync(0xffffffffu, alpha < 1.f)) {
@@ -923,15 +923,6 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
                 make_uint4(0, 0, 0, 0);
           }
           fence_proxy_async_smem();  // the MMA reads these rows through the async proxy
-        }
-        // P (bf16 pairs) over the first half of this tile's S buffer.
-        if (live) {
-          float pw[BN / 2];
-#pragma unroll
-          for (int i = 0; i < BN / 2; ++i)
-            pw[i] = __uint_as_float(pack_bf16x2(sv[2 * i], sv[2 * i + 1]));
-          static_assert(BN / 2 == 32, "P is written with one 32-column TMEM store");
-          tmem_store32(sp, pw);
         }
         tc_fence_before_sync();
         mbar_arrive(&p_full[2 * h + (gt & 1)]);
