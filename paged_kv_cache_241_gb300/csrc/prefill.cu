@@ -812,15 +812,28 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
           float mt;
           {
             float e0 = -INFINITY;
-            if (qs >= 0.f) {
+            if (qs > 0.f) {
               float vmax;
               tmem_load64_max(sp, sv, vmax);
               if (full_row) {
                 e0 = vmax;
               } else {
+                // Keys past the row's limit become -inf (their P is then
+                // exactly 0 in the unmasked exponential loop below).
+                const int nvis = key_limit - key0;
+                float e1 = -INFINITY, e2 = -INFINITY, e3 = -INFINITY;
 #pragma unroll
-                for (int i = 0; i < BN; ++i)
-                  if (key0 + i <= key_limit) e0 = fmaxf(e0, sv[i]);
+                for (int i = 0; i < BN; i += 4) {
+                  sv[i] = i <= nvis ? sv[i] : -INFINITY;
+                  sv[i + 1] = i + 1 <= nvis ? sv[i + 1] : -INFINITY;
+                  sv[i + 2] = i + 2 <= nvis ? sv[i + 2] : -INFINITY;
+                  sv[i + 3] = i + 3 <= nvis ? sv[i + 3] : -INFINITY;
+                  e0 = fmaxf(e0, sv[i]);
+                  e1 = fmaxf(e1, sv[i + 1]);
+                  e2 = fmaxf(e2, sv[i + 2]);
+                  e3 = fmaxf(e3, sv[i + 3]);
+                }
+                e0 = fmaxf(fmaxf(e0, e1), fmaxf(e2, e3));
               }
               mt = e0 * qs;
             } else {
@@ -846,9 +859,10 @@ __global__ void __launch_bounds__(threads_for<NH>(), 1)
             // while the next half is computed.
             const float2 q2 = make_float2(qs, qs), nm2 = make_float2(-m_ref, -m_ref);
             float2 r01 = make_float2(0.f, 0.f), r23 = make_float2(0.f, 0.f);
+            const bool dense = full_row || qs > 0.f;  // no mask to apply in the loop
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
-              if (full_row) {
+              if (dense) {
 #pragma unroll
                 for (int i = hf * (BN / 2); i < (hf + 1) * (BN / 2); i += 4) {
                   const float2 x01 = fma2(make_float2(sv[i], sv[i + 1]), q2, nm2);

@@ -2,6 +2,8 @@
 
 Tolerance: |gpu - oracle| <= 8e-3 + 1e-2 |oracle| elementwise (bf16 inputs,
 fp32 accumulation, bf16 output)."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -106,6 +108,20 @@ def test_decode_edge_lengths(lib, D, G):
     b = wl.build_batch("edge", "decode", 10 + G + D, [L - 1 for L in lens], [1] * len(lens),
                        G * Hkv, Hkv, D, num_blocks=40, max_blocks_pad=3)
     check_decode(lib, b)
+
+
+@pytest.mark.parametrize("scale", [0.0, -1.0 / np.sqrt(128.0)])
+@pytest.mark.parametrize("G", [2, 4])
+def test_decode_zero_and_negative_scale(lib, scale, G):
+    # A negative scale puts each row's largest scaled logit at its smallest
+    # q.k; zero gives the mean of the context's values.  Contexts across the
+    # 64-token tile and 256-token block boundaries, NaN in stale slots.
+    L = np.array([1, 63, 64, 65, 255, 256, 257, 700, 1500, 2048])
+    b = wl.build_batch("dscale", "decode", 17 + G, L - 1, np.ones(len(L), np.int64), 4 * G, 4,
+                       128, stale="nan")
+    b = dataclasses.replace(b, scale=float(scale))
+    db, out = check_decode(lib, b)
+    assert torch.isfinite(out.float()).all()
 
 
 @pytest.mark.parametrize("bs", [64, 128, 512])

@@ -1,6 +1,8 @@
 """Paged varlen causal prefill on the GPU (tcgen05 path) against the fp64 oracle.
 
 Tolerance: |gpu - oracle| <= 8e-3 + 1e-2 |oracle| elementwise."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -61,6 +63,25 @@ def test_prefill_packed_tiles(lib, D, G):
     cached = [(37 * i) % 700 for i in range(len(new))]
     b = wl.build_batch("packed", "prefill", 110 + D + G, cached, new, 2 * G, 2, D, stale="nan")
     assert b.q.shape[0] <= 128 * b.num_seqs and max(new) <= 1024
+    db, out = check_prefill(lib, b)
+    assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("scale", [0.0, -1.0 / np.sqrt(128.0)])
+@pytest.mark.parametrize("form", ["short", "long", "packed"])
+def test_prefill_zero_and_negative_scale(lib, scale, form):
+    # softmax(q K^T * scale) is defined for any scale.  A negative scale makes
+    # a row's largest scaled logit come from its smallest q.k (the kernel's
+    # minimum path instead of the load-with-max); zero gives the mean of the
+    # row's visible values.  Each batch selects one kernel form: short
+    # prompts (one MMA issuer per head), long prompts (the S / P.V issuer
+    # pair) and a decode-heavy batch (packed tiles); all cross the causal
+    # diagonal over cached prefixes, with ragged tails and NaN in stale slots.
+    cached, new = {"short": ([0, 256, 70], [300, 129, 64]),
+                   "long": ([0, 300], [1100, 1300]),
+                   "packed": ([5, 400, 0, 77, 1000, 256], [1, 1, 65, 1, 33, 129])}[form]
+    b = wl.build_batch("scale", "prefill", 91, cached, new, 4, 2, 128, stale="nan")
+    b = dataclasses.replace(b, scale=float(scale))
     db, out = check_prefill(lib, b)
     assert torch.isfinite(out.float()).all()
 
