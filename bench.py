@@ -593,21 +593,35 @@ def oracle_decode_steps(steps, warmup=1, batch=None):
     return sum(times) / len(times), b, pool.workers
 
 
-def oracle_prefill_sample(stride=32):
-    """TFLOP/s of the oracle on all host cores over a sample of the varlen
-    prefill workload (16 prompts, U[64, 4096] tokens, 16 q / 8 kv heads,
-    D 128): every `stride`-th query row of every prompt and its last row,
-    each sequence's sampled rows one pool task.  Flops count the sampled rows'
-    unmasked keys, as for the kernel.  Returns a cpu_baseline record."""
+SAMPLED_PREFILL = {
+    "prefill": (lambda: wl.prefill(), 32,
+                "16 prompts, U[64, 4096] tokens"),
+    "prefix": (lambda: wl.prefix(), 4,
+               "32 sequences, k*256 cached + U[1, 512] new tokens"),
+    "mixed": (lambda: wl.mixed(), 4,
+              "48 decode rows + 8 prompt chunks"),
+}
+
+
+def oracle_prefill_sample(name="prefill"):
+    """TFLOP/s of the oracle on all host cores over a sample of a prefill-
+    kernel workload (varlen prefill, prefix-cached prefill or the mixed step;
+    16 q / 8 kv heads, D 128): every `stride`-th query row of every sequence
+    and its last row, each sequence's sampled rows one pool task.  Flops
+    count the sampled rows' unmasked keys, as for the kernel.  Returns a
+    cpu_baseline record."""
     import oracle
 
-    b = wl.prefill()
+    make, stride, what = SAMPLED_PREFILL[name]
+    b = make()
     kc, vc = oracle.kv_store(b.k_cache, b.v_cache, b.k, b.v, b.slot_mapping)
     cu_q, cu_k = b.cu_seqlens_q, b.cu_seqlens_k
     tasks, pairs, nrows = [], 0, 0
     for s in range(b.num_seqs):
         q0, q1 = int(cu_q[s]), int(cu_q[s + 1])
         n, len_k = q1 - q0, int(cu_k[s + 1] - cu_k[s])
+        if n == 0:
+            continue
         rows = np.unique(np.concatenate([np.arange(0, n, stride), [n - 1]]))
         pairs += int(np.sum(len_k - n + rows + 1))
         nrows += len(rows)
@@ -623,8 +637,8 @@ def oracle_prefill_sample(stride=32):
     flops = 4 * b.head_dim * b.num_q_heads * pairs
     return {"value": flops / el / 1e12, "unit": "TFLOP/s", "cores": pool.workers,
             "kind": "oracle", "seconds": el,
-            "sample": f"prefill: one query row in {stride} and the last row of each of the 16 "
-                      f"prompts ({nrows} of {b.q.shape[0]} rows, all 16 heads)"}
+            "sample": f"{name}: one query row in {stride} and the last row of each sequence "
+                      f"({what}; {nrows} of {b.q.shape[0]} rows, all {b.num_q_heads} heads)"}
 
 
 # ------------------------------------------------------------ main
@@ -656,7 +670,9 @@ def run_reference(args):
                          "sample": "the whole decode batch every step (kv_store in one process, "
                                    "attention one sequence per worker task)"},
         "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-        "prefill": {"cpu_baseline": oracle_prefill_sample()},
+        "prefill": {"cpu_baseline": oracle_prefill_sample("prefill")},
+        "prefix": {"cpu_baseline": oracle_prefill_sample("prefix")},
+        "mixed": {"cpu_baseline": oracle_prefill_sample("mixed")},
     }
     print(json.dumps(line))
     return 0
@@ -847,8 +863,9 @@ def main():
                                 "unit": "GB/s", "cores": workers, "kind": "oracle",
                                 "sample": f"the whole 64-sequence decode batch, {steps} steps, "
                                           f"{per:.3f} s per step"}
-        if "prefill" in line:
-            line["prefill"]["cpu_baseline"] = oracle_prefill_sample()
+        for name in SAMPLED_PREFILL:
+            if name in line:
+                line[name]["cpu_baseline"] = oracle_prefill_sample(name)
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
