@@ -132,6 +132,9 @@ size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads
  * every entry before reading it).  Calls that overlap on the device must not
  * share a workspace.
  *
+ * scale: any finite value (zero averages the context's values; a NaN or
+ * infinite scale returns PKV_ERR_INVALID_ARG and launches nothing).
+ *
  * Supported: head_dim in {64, 128}; Hq/Hkv in {1, 2, 4, 8}; block_size in
  * {64, 128, 256, 512}; num_seqs <= 16384, and the kernel's per-CTA shared
  * memory (which holds every sequence's block offset and length) must fit in
@@ -255,6 +258,9 @@ pkv_status pkv_test_decode_fault(int64_t wait_limit_ns, int withhold_tile);
  * again, so one zero-fill at allocation is enough.  Calls that may run at the
  * same time on the GPU (other streams, other host threads) need workspaces
  * of their own.  Missing, short or misaligned: PKV_ERR_WORKSPACE.
+ *
+ * scale: any finite value (a NaN or infinite scale returns
+ * PKV_ERR_INVALID_ARG and launches nothing).
  *
  * Supported: head_dim in {64, 128}; Hq/Hkv in {1, 2, 4, 8};
  * block_size in {64, 128, 256, 512}.

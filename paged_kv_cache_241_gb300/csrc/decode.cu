@@ -1144,7 +1144,7 @@ pkv_status decode_call(uint16_t *out, const uint16_t *q, const uint16_t *k_cache
   if (block_size != 64 && block_size != 128 && block_size != 256 && block_size != 512)
     return PKV_ERR_UNSUPPORTED;
   if (num_seqs > kMaxSeqs) return PKV_ERR_UNSUPPORTED;
-  if (!(scale == scale)) return PKV_ERR_INVALID_ARG;
+  if (!isfinite(scale)) return PKV_ERR_INVALID_ARG;  // NaN or infinite
   if (num_seqs == 0) return PKV_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
     return PKV_ERR_INVALID_ARG;

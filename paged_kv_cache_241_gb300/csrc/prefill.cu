@@ -1019,7 +1019,7 @@ extern "C" pkv_status pkv_paged_prefill_attn(uint16_t *out, const uint16_t *q,
   if (G != 1 && G != 2 && G != 4 && G != 8) return PKV_ERR_UNSUPPORTED;
   if (block_size != 64 && block_size != 128 && block_size != 256 && block_size != 512)
     return PKV_ERR_UNSUPPORTED;
-  if (!(scale == scale)) return PKV_ERR_INVALID_ARG;
+  if (!isfinite(scale)) return PKV_ERR_INVALID_ARG;  // NaN or infinite
   if (num_seqs == 0 || total_q == 0 || max_seqlen_q == 0) return PKV_OK;
   if (total_q > 0x7FFFFFFFLL) return PKV_ERR_UNSUPPORTED;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !cu_seqlens_q || !cu_seqlens_k)

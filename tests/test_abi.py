@@ -98,6 +98,9 @@ def test_decode_rejects_bad_arguments(lib):
     assert decode_call(lib, BS=100) == 2                  # block size not built
     assert decode_call(lib, S=20000) == 2                 # too many sequences
     assert decode_call(lib, scale=float("nan")) == 1
+    for bad in (float("nan"), float("inf"), -float("inf")):   # checked before the empty batch
+        assert decode_call(lib, S=0, scale=bad) == 1
+    assert decode_call(lib, S=0, scale=0.0) == 0 and decode_call(lib, S=0, scale=-2.0) == 0
     assert decode_call(lib) == 1                          # null pointers
     p = ctypes.c_void_p(0x10000)
     # workspace missing / too small / misaligned
@@ -134,6 +137,9 @@ def test_prefill_rejects_bad_arguments(lib):
     assert prefill_call(lib, T=-1) == 1
     assert prefill_call(lib) == 1                         # null pointers
     assert prefill_call(lib, T=0) == 0                    # nothing to do
+    for bad in (float("nan"), float("inf"), -float("inf")):   # checked before the empty batch
+        assert prefill_call(lib, T=0, scale=bad) == 1
+    assert prefill_call(lib, T=0, scale=0.0) == 0 and prefill_call(lib, T=0, scale=-2.0) == 0
     # workspace missing / too small / misaligned
     p = ctypes.c_void_p(0x10000)
     ptrs = dict(out=p, q=p, kc=p, vc=p, bt=p, cq=p, ck=p)
